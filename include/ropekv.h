@@ -1,0 +1,183 @@
+/*
+ * ropekv.h -- C ABI of the fused RoPE + KV-cache write library (libropekv.so).
+ *
+ * One call = one CUDA kernel launch on the caller's stream that, for every
+ * token and head, reads the packed FP16 QKV row (or the K/V delta rows) and the
+ * FP32 cos/sin row of the token's position, rotates the first rotaryDim dims
+ * of Q and K, x' = x*cos + rotate(x)*sin, and writes rotated Q, rotated K and
+ * unchanged V. Sources (web pages, cited by title and section):
+ *
+ *   [ARW] TensorRT-Edge-LLM 0.4.0 C++ API, "Apply Rope Write KV"
+ *         (launchApplyRopeWriteKVPackedQKV, launchApplyRopeWriteKVContinuousQAndKVCache,
+ *         launchApplyRopeWriteKVTreeDecoding).
+ *   [DRK] TensorRT-Edge-LLM C++ API, "Dflash Runtime Kernels"
+ *         (launchDFlashTargetKVCacheUpdate, checkDFlashRopeCapacity).
+ *   [RC]  sglang rope_cache.py (_get_neox_rotated_x, _get_gptj_rotated_x,
+ *         _unit_rope, _load_cos_sin, kernel Stage 2.1).
+ *
+ * Common rules for every entry point:
+ *   - FP16 tensors are uint16_t arrays holding IEEE binary16 bits; FP32 tables
+ *     are float; indices are int32_t. All tensors are dense, row-major, in the
+ *     layouts stated per call.
+ *   - Every tensor pointer is a DEVICE pointer owned by the caller and must be
+ *     16-byte aligned. The library allocates nothing, keeps no state between
+ *     calls and never synchronises; results are ready when the stream says so.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream). Calls are asynchronous and may be captured in a CUDA graph.
+ *   - cos/sin rows hold rotaryDim floats: cos_0..cos_{r/2-1} then
+ *     sin_0..sin_{r/2-1} ([RC] _load_cos_sin and the half-width table rule).
+ *     Dims i and partner use frequency i: NeoX pairs (i, i + r/2), GPT-J pairs
+ *     (2i, 2i + 1) ([RC] rotate layouts and Stage 2.1). Dims >= rotaryDim and
+ *     all V heads are copied bit for bit.
+ *   - Return value: ROPEKV_OK (0), or a negative ropekv_status when the host
+ *     rejected the arguments (nothing launched) or the launch failed.
+ *     Data-dependent invalid indices found on the device (negative or
+ *     out-of-range positions, sequences, slots or pages) are skipped: nothing
+ *     is written for them, and no error is raised ([DRK] skip rules).
+ *   - Supported shapes: headDim in {64, 128, 256}; rotaryDim a multiple of 16
+ *     with 16 <= rotaryDim <= headDim; numQHeads a multiple of numKVHeads.
+ *     Element counts of every tensor must fit in int64.
+ *   - Two tokens that resolve to the same cache slot race (last writer wins
+ *     in no fixed order); the pages' producers never generate them.
+ */
+#ifndef ROPEKV_H
+#define ROPEKV_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define ROPEKV_API __attribute__((visibility("default")))
+#else
+#define ROPEKV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Pairing of rotated dims: GPT-NeoX half split or GPT-J interleaved pairs. */
+typedef enum { ROPEKV_NEOX = 0, ROPEKV_GPTJ = 1 } ropekv_style;
+
+typedef enum {
+    ROPEKV_OK = 0,
+    ROPEKV_ERR_NULL_POINTER = -1,    /* a required pointer is NULL              */
+    ROPEKV_ERR_MISALIGNED = -2,      /* a tensor pointer is not 16-byte aligned */
+    ROPEKV_ERR_HEAD_DIM = -3,        /* headDim not in {64, 128, 256}           */
+    ROPEKV_ERR_ROTARY_DIM = -4,      /* rotaryDim not a multiple of 16 in [16, headDim] */
+    ROPEKV_ERR_HEADS = -5,           /* numQHeads/numKVHeads <= 0 or not divisible */
+    ROPEKV_ERR_SHAPE = -6,           /* negative size, or a size too large       */
+    ROPEKV_ERR_COS_SIN_BATCH = -7,   /* cosSinBatch neither 1 nor batch          */
+    ROPEKV_ERR_CAPACITY = -8,        /* capacity check failed (see each call)    */
+    ROPEKV_ERR_STYLE = -9,           /* style not a ropekv_style                 */
+    ROPEKV_ERR_LAUNCH = -10          /* the CUDA launch reported an error        */
+} ropekv_status;
+
+/* Sizes of the contiguous-cache entry points ([ARW]). */
+typedef struct {
+    int32_t batch;        /* B: sequences                                        */
+    int32_t seqLen;       /* S: runtime tokens per sequence                      */
+    int32_t numQHeads;    /* Hq                                                  */
+    int32_t numKVHeads;   /* Hkv (= Hk = Hv)                                     */
+    int32_t headDim;      /* D                                                   */
+    int32_t rotaryDim;    /* r: leading dims of each Q/K head that are rotated   */
+    int32_t kvCapacity;   /* slots per sequence in the cache                     */
+    int32_t cosSinBatch;  /* 1 (one table for all sequences) or B (one per seq)  */
+    int32_t cosSinSeqLen; /* rows (positions) per table                          */
+    int32_t style;        /* a ropekv_style                                      */
+} ropekv_dims;
+
+/*
+ * [ARW] launchApplyRopeWriteKVPackedQKV: the cache is empty.
+ *   cosSin  [cosSinBatch, cosSinSeqLen, rotaryDim] FP32, read.
+ *   qkv     [B, S, Hq + 2*Hkv, headDim] FP16, heads ordered Q, K, V; read and
+ *           written IN PLACE: Q and K heads are rotated, V heads are left as is.
+ *   kvCache [B, 2, Hkv, kvCapacity, headDim] FP16, written: plane 0 = rotated K,
+ *           plane 1 = V, at slots 0..S-1 ("from the start positions"); token s
+ *           uses cos/sin row s. Slots >= S are not touched.
+ * Host errors: S > kvCapacity or S > cosSinSeqLen -> ROPEKV_ERR_CAPACITY.
+ */
+ROPEKV_API int rope_write_kv_packed(const float* cosSin, uint16_t* qkv, uint16_t* kvCache,
+                                    const ropekv_dims* dims, void* stream);
+
+/*
+ * [ARW] launchApplyRopeWriteKVContinuousQAndKVCache: the cache already holds
+ * tokens. kvCacheEndLens[b] is the end position after writing, so token s of
+ * sequence b takes slot = position = kvCacheEndLens[b] - S + s.
+ *   cosSin         [cosSinBatch, cosSinSeqLen, rotaryDim] FP32, read.
+ *   kvCacheEndLens [B] INT32, read on the device.
+ *   qkv            [B, S, Hq + 2*Hkv, headDim] FP16, read only.
+ *   kvCache        [B, 2, Hkv, kvCapacity, headDim] FP16, written at the slots.
+ *   qOut           [B, S, Hq, headDim] FP16, written (rotated Q).
+ * A token whose slot is < 0, >= kvCapacity or >= cosSinSeqLen writes nothing
+ * (neither its qOut row nor its cache slots).
+ */
+ROPEKV_API int rope_write_kv_continuous(const float* cosSin, const int32_t* kvCacheEndLens,
+                                        const uint16_t* qkv, uint16_t* kvCache,
+                                        uint16_t* qOut, const ropekv_dims* dims,
+                                        void* stream);
+
+/*
+ * [ARW] launchApplyRopeWriteKVTreeDecoding: tree attention for speculative
+ * decoding. As the continuous call, except that the RoPE position of token
+ * (b, s) is tokenPosIds[b, s] ("position of token within sequence"); the cache
+ * slot stays kvCacheEndLens[b] - S + s, so sibling nodes that share a position
+ * keep distinct slots.
+ *   tokenPosIds [B, S] INT32, read on the device.
+ * A token whose position is < 0 or >= cosSinSeqLen, or whose slot is outside
+ * [0, kvCapacity), writes nothing.
+ */
+ROPEKV_API int rope_write_kv_tree(const float* cosSin, const int32_t* kvCacheEndLens,
+                                  const int32_t* tokenPosIds, const uint16_t* qkv,
+                                  uint16_t* kvCache, uint16_t* qOut,
+                                  const ropekv_dims* dims, void* stream);
+
+/*
+ * [DRK] launchDFlashTargetKVCacheUpdate: RoPE on token-major K delta rows, and
+ * K/V delta rows written into their sequences' pages of a paged pool.
+ *   kDelta, vDelta        [numDeltaTokens, numKVHeads, headDim] FP16, read
+ *                         (K not yet rotated).
+ *   kvCache               [2, numPages, tokensPerPage, numKVHeads, headDim] FP16,
+ *                         written at the destinations below, untouched elsewhere.
+ *   tokenAlignedCosSin    [numDeltaTokens, rotaryDim] FP32: row t serves delta row t.
+ *   deltaPositions        [numDeltaTokens] INT32 absolute KV positions.
+ *   deltaTokenToSequence  [numDeltaTokens] INT32 owning sequence.
+ *   pageTable             [batchSize, 2, maxPagesPerSeq] INT32 canonical page ids:
+ *                         plane 0 entries in [0, numPages) name K pages, plane 1
+ *                         entries in [numPages, 2*numPages) name V pages; the id
+ *                         is the flat page index of the [2, numPages] pool.
+ * Row t with pos = deltaPositions[t], seq = deltaTokenToSequence[t] and logical
+ * page lp = pos / tokensPerPage writes rotated K to flat page
+ * pageTable[seq, 0, lp] and V to flat page pageTable[seq, 1, lp], both at
+ * in-page slot pos % tokensPerPage. The row is skipped when pos < 0, seq < 0,
+ * seq >= batchSize or lp >= maxPagesPerSeq; each plane is skipped on its own
+ * when its id is unmapped (negative) or outside that plane's range.
+ * tokensPerPage is a runtime argument here (a compile-time constant on the page).
+ * Host errors: tokensPerPage <= 0, numPages or maxPagesPerSeq < 0.
+ */
+ROPEKV_API int paged_kv_delta_update(const uint16_t* kDelta, const uint16_t* vDelta,
+                                     uint16_t* kvCache, const float* tokenAlignedCosSin,
+                                     const int32_t* deltaPositions,
+                                     const int32_t* deltaTokenToSequence,
+                                     const int32_t* pageTable, int32_t numDeltaTokens,
+                                     int32_t batchSize, int32_t numKVHeads, int32_t headDim,
+                                     int32_t rotaryDim, int32_t numPages,
+                                     int32_t maxPagesPerSeq, int32_t tokensPerPage,
+                                     int32_t style, void* stream);
+
+/*
+ * [DRK] checkDFlashRopeCapacity: the RoPE table must cover every position the
+ * paged update can write. kvCapacity is the page-aligned per-sequence capacity
+ * (maxPagesPerSeq * tokensPerPage); the table may be shorter than it, so only
+ * cosSinSeqLen > kvCapacity is rejected. Host only; returns ROPEKV_OK or
+ * ROPEKV_ERR_CAPACITY (the page's version throws instead).
+ */
+ROPEKV_API int rope_check_capacity(int32_t cosSinSeqLen, int32_t kvCapacity);
+
+/* Static, human-readable text for a status code (never NULL). */
+ROPEKV_API const char* ropekv_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ROPEKV_H */

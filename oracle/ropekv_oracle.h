@@ -1,0 +1,120 @@
+/*
+ * ropekv_oracle.h -- CPU oracle for the fused RoPE + KV-cache write.
+ *
+ * TEST INFRASTRUCTURE. This is the plain, slow, double-precision statement of
+ * what the fused RoPE + KV-cache write computes. Only the test suite, the
+ * smoke check and the benchmark's CPU-baseline leg may load it. The library's
+ * product path never calls it, and the two share no code, header, table or
+ * helper.
+ *
+ * Sources, cited by page title and section:
+ *   [ARW] TensorRT-Edge-LLM 0.4.0 C++ API, "Apply Rope Write KV":
+ *         launchApplyRopeWriteKVPackedQKV, launchApplyRopeWriteKVContinuousQAndKVCache,
+ *         launchApplyRopeWriteKVTreeDecoding (parameter lists: layouts, in/out roles).
+ *   [RC]  sglang python/sglang/kernels/ops/kvcache/rope_cache.py:
+ *         _get_neox_rotated_x, _get_gptj_rotated_x, _unit_rope, _load_cos_sin,
+ *         kernel Stage 2.1 (frequency index) and the wrapper's cos_sin width rule.
+ *   [DRK] TensorRT-Edge-LLM C++ API, "Dflash Runtime Kernels":
+ *         launchDFlashTargetKVCacheUpdate, checkDFlashRopeCapacity.
+ *
+ * Conventions shared by every function below:
+ *   - FP16 tensors are passed as uint16_t arrays of IEEE 754 binary16 bits.
+ *   - cos/sin rows hold r = rotaryDim FP32 values: cos_0..cos_{r/2-1} then
+ *     sin_0..sin_{r/2-1} ([RC] _load_cos_sin reads sin at the cos index plus
+ *     the frequency count; the wrapper's half-width rule fixes that count at r/2).
+ *   - style 0 = GPT-NeoX half split, style 1 = GPT-J interleaved pairs.
+ *   - All buffers are host memory owned by the caller. Functions return 0 on
+ *     success and -1 when the sizes are inconsistent (nothing is written then).
+ *
+ * Parity status: every function here is pinned by tests under tests/ (worked
+ * examples, closed forms, invariants and brute-force placement tables).
+ */
+#ifndef ROPEKV_ORACLE_H
+#define ROPEKV_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* IEEE 754 binary16 bits -> double (exact). */
+double ropekv_oracle_f16_to_f64(uint16_t bits);
+
+/* double -> IEEE 754 binary16 bits, round to nearest, ties to even;
+ * overflow goes to infinity, NaN stays NaN. */
+uint16_t ropekv_oracle_f64_to_f16(double x);
+
+/* rotate(x) of [RC] _get_neox_rotated_x / _get_gptj_rotated_x over the first
+ * r dims of one head: NeoX [x0,x1,x2,x3] -> [-x2,-x3,x0,x1],
+ * GPT-J [x0,x1,x2,x3] -> [-x1,x0,-x3,x2]. Writes out[0..r). */
+void ropekv_oracle_rotate_half(const double* x, int r, int style, double* out);
+
+/* Frequency index of dim d (< r), [RC] kernel Stage 2.1 with the half-width
+ * table: NeoX d mod (r/2), GPT-J d / 2. */
+int ropekv_oracle_freq_index(int d, int r, int style);
+
+/* [RC] _unit_rope on one head, in double: y[d] = x[d]*cos[f(d)] + rotate(x)[d]*sin[f(d)]
+ * for d < r; y[d] = x[d] for r <= d < D. cs_row is the r-float table row. */
+void ropekv_oracle_rope_head_f64(const double* x, const float* cs_row, int D, int r,
+                                 int style, double* y);
+
+/* [ARW] launchApplyRopeWriteKVPackedQKV. Empty cache: position = cache slot = s.
+ * qkv [B,S,Hq+2Hkv,D] is rotated in place (Q and K heads; V heads untouched),
+ * kvCache [B,2,Hkv,cap,D] receives rotated K (plane 0) and V bits (plane 1) at
+ * slots 0..S-1. cosSin [csBatch,csSeq,r]; csBatch is 1 (shared) or B. */
+int ropekv_oracle_packed(const float* cosSin, uint16_t* qkv, uint16_t* kvCache,
+                         int B, int S, int Hq, int Hkv, int D, int r, int cap,
+                         int csBatch, int csSeq, int style);
+
+/* [ARW] launchApplyRopeWriteKVContinuousQAndKVCache. slot = pos =
+ * kvCacheEndLens[b] - S + s. qkv is read only; rotated Q goes to qOut
+ * [B,S,Hq,D]; rotated K and V bits go to the cache at slot. A token whose slot
+ * is negative, >= cap or >= csSeq writes nothing. */
+int ropekv_oracle_continuous(const float* cosSin, const int32_t* kvCacheEndLens,
+                             const uint16_t* qkv, uint16_t* kvCache, uint16_t* qOut,
+                             int B, int S, int Hq, int Hkv, int D, int r, int cap,
+                             int csBatch, int csSeq, int style);
+
+/* [ARW] launchApplyRopeWriteKVTreeDecoding. RoPE position = tokenPosIds[b,s];
+ * cache slot = kvCacheEndLens[b] - S + s (linear order). A token with a
+ * negative or >= csSeq position, or a slot outside [0,cap), writes nothing. */
+int ropekv_oracle_tree(const float* cosSin, const int32_t* kvCacheEndLens,
+                       const int32_t* tokenPosIds, const uint16_t* qkv,
+                       uint16_t* kvCache, uint16_t* qOut,
+                       int B, int S, int Hq, int Hkv, int D, int r, int cap,
+                       int csBatch, int csSeq, int style);
+
+/* [DRK] launchDFlashTargetKVCacheUpdate, per delta row, without a pool.
+ * For row t: kDest[t] / vDest[t] receive the element offset, inside a pool laid
+ * out [2, numPages, tokensPerPage, Hkv, D], of the row's [Hkv, D] block in the
+ * K / V plane, or -1 when that plane is skipped. kOut / vOut [numDeltaTokens,Hkv,D]
+ * receive the values written there (rotated K with cos/sin row t; V bits);
+ * rows whose plane is skipped are left as they were. */
+int ropekv_oracle_paged_rows(const uint16_t* kDelta, const uint16_t* vDelta,
+                             const float* tokenAlignedCosSin,
+                             const int32_t* deltaPositions, const int32_t* deltaTokenToSequence,
+                             const int32_t* pageTable,
+                             int numDeltaTokens, int batchSize, int Hkv, int D, int r,
+                             int numPages, int maxPagesPerSeq, int tokensPerPage, int style,
+                             int64_t* kDest, int64_t* vDest, uint16_t* kOut, uint16_t* vOut);
+
+/* [DRK] launchDFlashTargetKVCacheUpdate into a host pool
+ * kvCache [2, numPages, tokensPerPage, Hkv, D]: the rows above, stored at their
+ * destinations. */
+int ropekv_oracle_paged(const uint16_t* kDelta, const uint16_t* vDelta, uint16_t* kvCache,
+                        const float* tokenAlignedCosSin,
+                        const int32_t* deltaPositions, const int32_t* deltaTokenToSequence,
+                        const int32_t* pageTable,
+                        int numDeltaTokens, int batchSize, int Hkv, int D, int r,
+                        int numPages, int maxPagesPerSeq, int tokensPerPage, int style);
+
+/* [DRK] checkDFlashRopeCapacity: 1 when the pair is rejected
+ * (cosSinSeqLen > kvCapacity), else 0. */
+int ropekv_oracle_capacity_rejected(int32_t cosSinSeqLen, int32_t kvCapacity);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ROPEKV_ORACLE_H */

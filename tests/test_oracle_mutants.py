@@ -1,0 +1,83 @@
+"""The oracle's pins catch planted mistakes.
+
+Each case copies the oracle's C source, plants one plausible mistake (a
+dropped term, a wrong sign or partner, a wrong index, a slot off by one, ...),
+builds it into a temporary library and runs the oracle pin tests against that
+build in a child process. Every mutant must make at least one pin fail. The
+real oracle is never modified; everything here runs on the CPU.
+"""
+import os
+import shutil
+import subprocess
+import sys
+import tempfile
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "ropekv_oracle.c")
+HDR = os.path.join(ROOT, "oracle", "ropekv_oracle.h")
+PIN_TESTS = ["tests/test_oracle_rope.py", "tests/test_oracle_entries.py",
+             "tests/test_oracle_fp16.py"]
+
+MUTANTS = {
+    "neox_rotate_sign": ("out[d] = (d < h) ? -x[d + h] : x[d - h];",
+                         "out[d] = (d < h) ? x[d + h] : x[d - h];"),
+    "gptj_rotate_partner": ("out[d] = (d % 2 == 0) ? -x[d + 1] : x[d - 1];",
+                            "out[d] = (d % 2 == 0) ? -x[d + 1] : -x[d - 1];"),
+    "neox_freq_index": ("return (style == STYLE_NEOX) ? (d % h) : (d / 2);",
+                        "return (style == STYLE_NEOX) ? (d / 2) : (d / 2);"),
+    "gptj_freq_index": ("return (style == STYLE_NEOX) ? (d % h) : (d / 2);",
+                        "return (style == STYLE_NEOX) ? (d % h) : (d % h);"),
+    "cos_sin_swapped": ("double c = (double)cs_row[f];\n        double s = (double)cs_row[h + f];",
+                        "double c = (double)cs_row[h + f];\n        double s = (double)cs_row[f];"),
+    "dropped_sin_term": ("y[d] = x[d] * c + rot[d] * s;", "y[d] = x[d] * c;"),
+    "rounding_truncates": ("double q = nearbyint(ldexp(a, 10 - E));",
+                           "double q = floor(ldexp(a, 10 - E));"),
+    "subnormal_scale": ("double k = nearbyint(ldexp(a, 24));",
+                        "double k = nearbyint(ldexp(a, 23));"),
+    "continuous_slot_off_by_one": (
+        "long long slot = (long long)kvCacheEndLens[b] - S + s;\n            long long pos = slot;",
+        "long long slot = (long long)kvCacheEndLens[b] - S + s + 1;\n            long long pos = slot;"),
+    "tree_position_from_slot": ("long long pos = tokenPosIds[(size_t)b * S + s];",
+                                "long long pos = (long long)kvCacheEndLens[b] - S + s;"),
+    "v_from_k_head": ("qkv_tok + (size_t)(Hq + Hkv + hv) * D",
+                      "qkv_tok + (size_t)(Hq + hv) * D"),
+    "packed_k_not_in_place": ("if (k_in_place)", "if (0)"),
+    "paged_row_by_position": ("tokenAlignedCosSin + (size_t)t * r;",
+                              "tokenAlignedCosSin + (size_t)(pos % numDeltaTokens) * r;"),
+    "paged_v_plane_unchecked": ("if (idV >= numPages && (int64_t)idV < 2 * (int64_t)numPages)",
+                                "if (idV >= 0 && (int64_t)idV < 2 * (int64_t)numPages)"),
+    "paged_capacity_unchecked": ("if (lp >= maxPagesPerSeq)", "if (lp > maxPagesPerSeq)"),
+    "capacity_rule_inclusive": ("return cosSinSeqLen > kvCapacity ? 1 : 0;",
+                                "return cosSinSeqLen >= kvCapacity ? 1 : 0;"),
+}
+
+
+@pytest.fixture(scope="module")
+def workdir():
+    d = tempfile.mkdtemp(prefix="ropekv_mutants_")
+    yield d
+    shutil.rmtree(d, ignore_errors=True)
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, workdir):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
+    mdir = os.path.join(workdir, name)
+    os.makedirs(mdir, exist_ok=True)
+    shutil.copy(HDR, mdir)
+    msrc = os.path.join(mdir, "ropekv_oracle.c")
+    with open(msrc, "w") as f:
+        f.write(src.replace(old, new))
+    lib = os.path.join(mdir, "libmutant.so")
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+                    "-o", lib, msrc, "-lm"], check=True)
+    env = dict(os.environ, ROPEKV_ORACLE_LIB=lib)
+    proc = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                           *PIN_TESTS], cwd=ROOT, env=env, capture_output=True, text=True,
+                          timeout=600)
+    assert proc.returncode != 0, f"mutant {name} passed every pin:\n{proc.stdout[-2000:]}"
+    assert "failed" in proc.stdout or "error" in proc.stdout.lower()

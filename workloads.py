@@ -1,0 +1,338 @@
+"""Seeded synthetic inputs for the fused RoPE + KV-cache write.
+
+This module only draws inputs: FP16 activations, cos/sin tables, positions,
+trees, page tables. It holds none of the rotation or cache-write arithmetic,
+and both the CUDA path's tests/benchmark and the CPU oracle's tests take their
+inputs from here. Every draw uses ``numpy.random.Generator(PCG64(seed))``.
+
+Workload shapes follow the pages: Llama-style GQA (32 query heads, 8 KV heads,
+head dim 128) for prefill, decode, tree speculative decoding (TensorRT-Edge-LLM
+"Apply Rope Write KV") and the DFlash paged delta update (TensorRT-Edge-LLM
+"Dflash Runtime Kernels", ``launchDFlashTargetKVCacheUpdate``). No dataset or
+trained weight is involved; activations are N(0,1) rounded to FP16.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+from typing import Optional
+
+import numpy as np
+
+NEOX = 0
+GPTJ = 1
+
+# FP16 bit pattern written into every output buffer before a call: a NaN that
+# no finite input or rotated value can produce, so any byte the call did not
+# write is recognisable afterwards.
+SENTINEL = 0x7E5A
+
+
+def rng_for(seed: int) -> np.random.Generator:
+    return np.random.Generator(np.random.PCG64(seed))
+
+
+def fp16_normal(rng: np.random.Generator, shape) -> np.ndarray:
+    """N(0,1) samples rounded to FP16 (numpy's round-to-nearest-even), as bits."""
+    return rng.standard_normal(size=shape).astype(np.float16).view(np.uint16)
+
+
+def cos_sin_table(theta: float, seq_len: int, rotary_dim: int, batch: int = 1,
+                  pos_offset: Optional[np.ndarray] = None) -> np.ndarray:
+    """FP32 table [batch, seq_len, rotary_dim] = [cos_0..cos_{h-1} | sin_0..sin_{h-1}].
+
+    Row p holds angle p * theta^(-2i/r) for frequency i < h = r/2, computed in
+    double and rounded to FP32. ``pos_offset`` (per batch row) shifts the
+    positions of each batch row, giving distinct per-sequence tables.
+    """
+    h = rotary_dim // 2
+    i = np.arange(h, dtype=np.float64)
+    inv_freq = theta ** (-(2.0 * i) / rotary_dim)
+    out = np.empty((batch, seq_len, rotary_dim), dtype=np.float32)
+    for b in range(batch):
+        off = 0 if pos_offset is None else int(pos_offset[b])
+        pos = np.arange(seq_len, dtype=np.float64) + off
+        ang = pos[:, None] * inv_freq[None, :]
+        out[b, :, :h] = np.cos(ang).astype(np.float32)
+        out[b, :, h:] = np.sin(ang).astype(np.float32)
+    return out
+
+
+def sentinel_fill(shape) -> np.ndarray:
+    return np.full(shape, SENTINEL, dtype=np.uint16)
+
+
+# ------------------------------------------------------------- contiguous --
+
+@dataclass
+class ContiguousCase:
+    """Inputs of the packed / continuous / tree entry points (host arrays)."""
+    mode: str                 # "packed" | "continuous" | "tree"
+    B: int
+    S: int
+    Hq: int
+    Hkv: int
+    D: int
+    r: int
+    cap: int
+    style: int
+    theta: float
+    cos_sin: np.ndarray       # [csB, csS, r] float32
+    qkv: np.ndarray           # [B, S, Hq+2Hkv, D] uint16
+    end_lens: Optional[np.ndarray] = None   # [B] int32
+    pos_ids: Optional[np.ndarray] = None    # [B, S] int32
+    cache_init: str = "sentinel"            # "sentinel" | "zero"
+    name: str = ""
+
+    @property
+    def H(self) -> int:
+        return self.Hq + 2 * self.Hkv
+
+    @property
+    def tokens(self) -> int:
+        return self.B * self.S
+
+    def new_cache(self) -> np.ndarray:
+        shape = (self.B, 2, self.Hkv, self.cap, self.D)
+        if self.cache_init == "zero":
+            return np.zeros(shape, dtype=np.uint16)
+        return sentinel_fill(shape)
+
+    def new_qout(self) -> np.ndarray:
+        return sentinel_fill((self.B, self.S, self.Hq, self.D))
+
+    def algorithmic_bytes(self) -> int:
+        """QKV read + cos/sin read (one row per token) + Q, K, V written."""
+        per_tok = (self.H * self.D * 2            # packed QKV row read
+                   + self.r * 4                   # cos/sin row read
+                   + self.Hq * self.D * 2         # Q written (qOut, or in place)
+                   + 2 * self.Hkv * self.D * 2)   # K and V cache rows written
+        if self.mode == "packed":
+            per_tok += self.Hkv * self.D * 2      # K also rotated in place in qkv
+        return per_tok * self.tokens
+
+
+def random_tree_depths(rng: np.random.Generator, n: int, max_parent_depth: int = 5) -> np.ndarray:
+    """Depths of a random tree of n nodes: node 0 is the root (depth 0); node
+    i > 0 picks its parent uniformly among earlier nodes of depth <= max_parent_depth."""
+    depth = np.zeros(n, dtype=np.int32)
+    for i in range(1, n):
+        cands = np.nonzero(depth[:i] <= max_parent_depth)[0]
+        parent = int(cands[rng.integers(0, len(cands))])
+        depth[i] = depth[parent] + 1
+    return depth
+
+
+def make_packed(B, S, Hq, Hkv, D, r, cap, style, theta, seed, cs_seq=None, cs_batch=1,
+                cache_init="zero", name="packed") -> ContiguousCase:
+    rng = rng_for(seed)
+    qkv = fp16_normal(rng, (B, S, Hq + 2 * Hkv, D))
+    cs_seq = cap if cs_seq is None else cs_seq
+    offs = None if cs_batch == 1 else rng.integers(0, 1000, size=cs_batch)
+    cos_sin = cos_sin_table(theta, cs_seq, r, cs_batch, offs)
+    return ContiguousCase("packed", B, S, Hq, Hkv, D, r, cap, style, theta, cos_sin, qkv,
+                          cache_init=cache_init, name=name)
+
+
+def make_continuous(B, S, Hq, Hkv, D, r, cap, style, theta, seed, end_lens=None,
+                    start_range=None, cs_seq=None, cs_batch=1, name="continuous") -> ContiguousCase:
+    """kvCacheEndLens = start_b + S with start_b uniform in start_range (inclusive),
+    unless ``end_lens`` is given."""
+    rng = rng_for(seed)
+    qkv = fp16_normal(rng, (B, S, Hq + 2 * Hkv, D))
+    if end_lens is None:
+        lo, hi = start_range if start_range is not None else (0, cap - S)
+        end_lens = rng.integers(lo, hi + 1, size=B).astype(np.int32) + np.int32(S)
+    end_lens = np.asarray(end_lens, dtype=np.int32)
+    cs_seq = cap if cs_seq is None else cs_seq
+    offs = None if cs_batch == 1 else rng.integers(0, 1000, size=cs_batch)
+    cos_sin = cos_sin_table(theta, cs_seq, r, cs_batch, offs)
+    return ContiguousCase("continuous", B, S, Hq, Hkv, D, r, cap, style, theta, cos_sin, qkv,
+                          end_lens=end_lens, name=name)
+
+
+def make_tree(B, S, Hq, Hkv, D, r, cap, style, theta, seed, base_range, cs_seq=None,
+              cs_batch=1, name="tree") -> ContiguousCase:
+    """tokenPosIds[b, s] = base_b + depth_b[s] over a random tree per sequence;
+    kvCacheEndLens[b] = base_b + S (tree tokens take linear slots)."""
+    rng = rng_for(seed)
+    qkv = fp16_normal(rng, (B, S, Hq + 2 * Hkv, D))
+    base = rng.integers(base_range[0], base_range[1] + 1, size=B).astype(np.int32)
+    depths = np.stack([random_tree_depths(rng, S) for _ in range(B)]) if S > 0 else \
+        np.zeros((B, 0), dtype=np.int32)
+    pos_ids = (base[:, None] + depths).astype(np.int32)
+    end_lens = (base + S).astype(np.int32)
+    cs_seq = cap if cs_seq is None else cs_seq
+    offs = None if cs_batch == 1 else rng.integers(0, 1000, size=cs_batch)
+    cos_sin = cos_sin_table(theta, cs_seq, r, cs_batch, offs)
+    return ContiguousCase("tree", B, S, Hq, Hkv, D, r, cap, style, theta, cos_sin, qkv,
+                          end_lens=end_lens, pos_ids=np.ascontiguousarray(pos_ids), name=name)
+
+
+# ------------------------------------------------------------------ paged --
+
+@dataclass
+class PagedCase:
+    """Inputs of the paged delta update (host arrays)."""
+    N: int                    # numDeltaTokens
+    B: int                    # batchSize
+    Hkv: int
+    D: int
+    r: int
+    num_pages: int
+    max_pages_per_seq: int
+    tokens_per_page: int
+    style: int
+    theta: float
+    k_delta: np.ndarray       # [N, Hkv, D] uint16
+    v_delta: np.ndarray       # [N, Hkv, D] uint16
+    cos_sin_rows: np.ndarray  # [N, r] float32 (token-aligned: row t for delta row t)
+    positions: np.ndarray     # [N] int32
+    seq_ids: np.ndarray       # [N] int32
+    page_table: np.ndarray    # [B, 2, maxPagesPerSeq] int32
+    name: str = ""
+    extra: dict = field(default_factory=dict)
+
+    def pool_shape(self):
+        return (2, self.num_pages, self.tokens_per_page, self.Hkv, self.D)
+
+    def new_pool(self) -> np.ndarray:
+        return sentinel_fill(self.pool_shape())
+
+    def plane_written(self):
+        """Boolean [N] masks: K plane written, V plane written (skip rules of
+        launchDFlashTargetKVCacheUpdate); input bookkeeping for byte counts."""
+        pos, seq = self.positions, self.seq_ids
+        ok = (pos >= 0) & (seq >= 0) & (seq < self.B)
+        lp = np.where(ok, pos // self.tokens_per_page, 0)
+        ok &= lp < self.max_pages_per_seq
+        s = np.where(ok, seq, 0)
+        lpc = np.where(ok, lp, 0)
+        idk = self.page_table[s, 0, lpc]
+        idv = self.page_table[s, 1, lpc]
+        kw = ok & (idk >= 0) & (idk < self.num_pages)
+        vw = ok & (idv >= self.num_pages) & (idv < 2 * self.num_pages)
+        return kw, vw
+
+    def algorithmic_bytes(self) -> int:
+        """Per row: 8 B of metadata; per written K plane: K read + cos/sin row +
+        K written; per written V plane: V read + V written."""
+        kw, vw = self.plane_written()
+        row = self.Hkv * self.D * 2
+        return int(self.N * 8 + kw.sum() * (2 * row + self.r * 4) + vw.sum() * 2 * row)
+
+    @property
+    def valid_rows(self) -> int:
+        kw, vw = self.plane_written()
+        return int((kw | vw).sum())
+
+
+def make_paged(N, B, Hkv, D, r, tokens_per_page, max_pages_per_seq, num_pages, style, theta,
+               seed, valid_rows=None, len_range=(1, 256), unmapped_frac=0.02,
+               max_position=None, name="paged") -> PagedCase:
+    """DFlash-style delta rows.
+
+    * per-sequence delta lengths L_b uniform in len_range, then moved by +-1 on
+      random sequences until sum(L_b) == valid_rows (default 95 % of N);
+    * the N - valid_rows padding rows (position = sequence = -1) sit at random
+      row indices; valid rows are grouped by sequence in order;
+    * sequence b's rows take consecutive positions old_b .. old_b + L_b - 1 with
+      old_b uniform in [0, max_position - L_b];
+    * K-plane page ids are a random permutation of [0, num_pages) spread over
+      the [B, maxPagesPerSeq] logical pages (cycled if there are more logical
+      pages than physical); V-plane ids are num_pages + a separate permutation;
+      then ``unmapped_frac`` of all table entries become -1;
+    * cos/sin rows are gathered at each row's position (padding rows zero).
+    """
+    rng = rng_for(seed)
+    if valid_rows is None:
+        valid_rows = int(round(0.95 * N))
+    if max_position is None:
+        max_position = max_pages_per_seq * tokens_per_page
+    lo, hi = len_range
+    hi = min(hi, max_position)
+    k_delta = fp16_normal(rng, (N, Hkv, D))
+    v_delta = fp16_normal(rng, (N, Hkv, D))
+    if B > 0:
+        L = rng.integers(lo, hi + 1, size=B).astype(np.int64)
+        if not (B * lo <= valid_rows <= B * hi):
+            raise ValueError("valid_rows not reachable with len_range")
+        while L.sum() != valid_rows:
+            b = int(rng.integers(0, B))
+            if L.sum() > valid_rows and L[b] > lo:
+                L[b] -= 1
+            elif L.sum() < valid_rows and L[b] < hi:
+                L[b] += 1
+    else:
+        L = np.zeros(0, dtype=np.int64)
+        valid_rows = 0
+    old = np.array([rng.integers(0, max_position - int(l) + 1) for l in L], dtype=np.int64)
+    seq_of_valid = np.repeat(np.arange(B, dtype=np.int32), L)
+    pos_of_valid = np.concatenate([old[b] + np.arange(L[b]) for b in range(B)]).astype(np.int32) \
+        if B > 0 else np.zeros(0, dtype=np.int32)
+    pad_idx = np.sort(rng.choice(N, size=N - valid_rows, replace=False))
+    is_pad = np.zeros(N, dtype=bool)
+    is_pad[pad_idx] = True
+    positions = np.full(N, -1, dtype=np.int32)
+    seq_ids = np.full(N, -1, dtype=np.int32)
+    positions[~is_pad] = pos_of_valid
+    seq_ids[~is_pad] = seq_of_valid
+    n_logical = B * max_pages_per_seq
+    reps = -(-n_logical // max(num_pages, 1)) if num_pages > 0 else 0
+    if num_pages > 0:
+        kperm = np.concatenate([rng.permutation(num_pages) for _ in range(reps)])[:n_logical]
+        vperm = np.concatenate([rng.permutation(num_pages) for _ in range(reps)])[:n_logical]
+    else:
+        kperm = np.full(n_logical, -1)
+        vperm = np.full(n_logical, -1 - num_pages)
+    table = np.empty((B, 2, max_pages_per_seq), dtype=np.int32)
+    table[:, 0, :] = kperm.reshape(B, max_pages_per_seq)
+    table[:, 1, :] = (vperm + num_pages).reshape(B, max_pages_per_seq)
+    n_unmapped = int(round(unmapped_frac * table.size))
+    if n_unmapped:
+        flat = table.reshape(-1)
+        flat[rng.choice(table.size, size=n_unmapped, replace=False)] = -1
+    cs_full = cos_sin_table(theta, max_position, r)[0]
+    cs_rows = np.zeros((N, r), dtype=np.float32)
+    valid = positions >= 0
+    cs_rows[valid] = cs_full[positions[valid]]
+    return PagedCase(N, B, Hkv, D, r, num_pages, max_pages_per_seq, tokens_per_page, style, theta,
+                     k_delta, v_delta, cs_rows, positions, seq_ids,
+                     np.ascontiguousarray(table), name=name, extra={"lengths": L, "old": old})
+
+
+# ------------------------------------------------------------ the configs --
+
+CONFIG_NAMES = ("packed_tiny", "prefill", "decode", "tree", "paged")
+
+
+def config(name: str):
+    """The five benchmark workloads, each drawn with its own seed (0..4)."""
+    if name == "packed_tiny":
+        # B=1, S=16, Hq=4, Hkv=2, D=r=64 NeoX, theta 1e4, table [1,64,64],
+        # zero-initialised cache [1,2,2,64,64], positions 0..15.
+        return make_packed(1, 16, 4, 2, 64, 64, 64, NEOX, 1e4, seed=0, cs_seq=64,
+                           cache_init="zero", name=name)
+    if name == "prefill":
+        # Llama-3-8B-shaped prefill: B=4, S=2048, Hq=32, Hkv=8, D=r=128 NeoX,
+        # theta 5e5, capacity 8192, end = start + 2048 with start in [0, 4096].
+        return make_continuous(4, 2048, 32, 8, 128, 128, 8192, NEOX, 5e5, seed=1,
+                               start_range=(0, 4096), cs_seq=8192, name=name)
+    if name == "decode":
+        # B=256 one-token decode, end lengths uniform in [1, 8192].
+        rng = rng_for(2)
+        qkv = fp16_normal(rng, (256, 1, 48, 128))
+        end_lens = rng.integers(1, 8192 + 1, size=256).astype(np.int32)
+        cos_sin = cos_sin_table(5e5, 8192, 128)
+        return ContiguousCase("continuous", 256, 1, 32, 8, 128, 128, 8192, NEOX, 5e5, cos_sin,
+                              qkv, end_lens=end_lens, name=name)
+    if name == "tree":
+        # B=64, 64 tree tokens, D=128, partial r=64 GPT-J, theta 1e4, base in
+        # [128, 4000], capacity 4096.
+        return make_tree(64, 64, 32, 8, 128, 64, 4096, GPTJ, 1e4, seed=3,
+                         base_range=(128, 4000), cs_seq=4096, name=name)
+    if name == "paged":
+        # 16384 delta rows over 128 sequences (15565 valid), Hkv=8, D=r=128,
+        # 64 tokens/page, 512 logical pages per sequence, 65536 pages per plane.
+        return make_paged(16384, 128, 8, 128, 128, 64, 512, 65536, NEOX, 5e5, seed=4,
+                          valid_rows=15565, name=name)
+    raise KeyError(name)
