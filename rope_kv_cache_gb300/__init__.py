@@ -1,0 +1,26 @@
+"""Fused RoPE + KV-cache write for GB300 (sm_103a).
+
+The compute lives in ``lib/libropekv.so`` (C ABI: ``include/ropekv.h``; kernels:
+``csrc/``). This package is its Python binding: functions with the entry
+points' names that take torch CUDA tensors and launch on the current stream.
+"""
+from ._binding import (  # noqa: F401
+    GPTJ,
+    NEOX,
+    LIB_PATH,
+    RopeKVError,
+    library_path,
+    load_library,
+    paged_kv_delta_update,
+    rope_check_capacity,
+    rope_write_kv_continuous,
+    rope_write_kv_packed,
+    rope_write_kv_tree,
+    ropekv_status_string,
+)
+
+__all__ = [
+    "NEOX", "GPTJ", "RopeKVError", "load_library", "library_path",
+    "rope_write_kv_packed", "rope_write_kv_continuous", "rope_write_kv_tree",
+    "paged_kv_delta_update", "rope_check_capacity", "ropekv_status_string",
+]

@@ -1,0 +1,223 @@
+"""ctypes binding of libropekv.so.
+
+Each function has the name of the C entry point it calls (include/ropekv.h),
+takes torch CUDA tensors in the layouts the header states, checks dtype,
+device, contiguity and shape agreement, and passes raw device pointers, the
+sizes read from the shapes and the current (or given) stream. It does no
+computation: every step runs in the library's kernels. A non-zero status
+raises RopeKVError. There is no fallback: without the built library the import
+of the functions fails loudly.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+NEOX = 0
+GPTJ = 1
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "lib", "libropekv.so")
+
+_lib = None
+
+
+class RopeKVError(RuntimeError):
+    """A non-zero status from libropekv.so."""
+
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn}: status {status} ({ropekv_status_string(status)})")
+
+
+class ropekv_dims(ctypes.Structure):
+    _fields_ = [(name, ctypes.c_int32) for name in (
+        "batch", "seqLen", "numQHeads", "numKVHeads", "headDim", "rotaryDim",
+        "kvCapacity", "cosSinBatch", "cosSinSeqLen", "style")]
+
+
+def library_path() -> str:
+    return LIB_PATH
+
+
+def load_library():
+    """Load libropekv.so once. Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(
+            f"{LIB_PATH} is not built; run `python -c \"import __graft_entry__ as g; g.build()\"` "
+            "(needs nvcc) -- there is no CPU fallback")
+    lib = ctypes.CDLL(LIB_PATH)
+    P = ctypes.c_void_p
+    I32 = ctypes.c_int32
+    D = ctypes.POINTER(ropekv_dims)
+    lib.rope_write_kv_packed.argtypes = [P, P, P, D, P]
+    lib.rope_write_kv_continuous.argtypes = [P, P, P, P, P, D, P]
+    lib.rope_write_kv_tree.argtypes = [P, P, P, P, P, P, D, P]
+    lib.paged_kv_delta_update.argtypes = [P] * 7 + [I32] * 9 + [P]
+    lib.rope_check_capacity.argtypes = [I32, I32]
+    lib.ropekv_status_string.argtypes = [ctypes.c_int]
+    lib.ropekv_status_string.restype = ctypes.c_char_p
+    for fn in ("rope_write_kv_packed", "rope_write_kv_continuous", "rope_write_kv_tree",
+               "paged_kv_delta_update", "rope_check_capacity"):
+        getattr(lib, fn).restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def ropekv_status_string(status: int) -> str:
+    return load_library().ropekv_status_string(int(status)).decode()
+
+
+def rope_check_capacity(cos_sin_seq_len: int, kv_capacity: int) -> None:
+    """Raise RopeKVError when the cos/sin table is longer than the capacity."""
+    rc = load_library().rope_check_capacity(int(cos_sin_seq_len), int(kv_capacity))
+    if rc != 0:
+        raise RopeKVError("rope_check_capacity", rc)
+
+
+# ------------------------------------------------------------- marshalling --
+
+def _dev_ptr(t: Optional[torch.Tensor], name: str, dtypes, device) -> ctypes.c_void_p:
+    if t is None:
+        return ctypes.c_void_p(0)
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name}: dtype {t.dtype} not in {dtypes}")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor (got {t.device})")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+_F16 = (torch.float16, torch.int16)
+_F32 = (torch.float32,)
+_I32 = (torch.int32,)
+
+
+def _stream_handle(stream, device) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check_rc(fn: str, rc: int) -> None:
+    if rc != 0:
+        raise RopeKVError(fn, rc)
+
+
+def _contiguous_dims(cos_sin, qkv, kv_cache, num_q_heads, num_kv_heads, style) -> ropekv_dims:
+    if cos_sin.dim() != 3 or qkv.dim() != 4 or kv_cache.dim() != 5:
+        raise ValueError("cos_sin [csB,csS,r], qkv [B,S,H,D], kv_cache [B,2,Hkv,cap,D] expected")
+    B, S, H, D = qkv.shape
+    if H != num_q_heads + 2 * num_kv_heads:
+        raise ValueError(f"qkv has {H} heads, expected Hq + 2*Hkv = {num_q_heads + 2 * num_kv_heads}")
+    if kv_cache.shape[0] != B or kv_cache.shape[1] != 2 or kv_cache.shape[2] != num_kv_heads \
+            or kv_cache.shape[4] != D:
+        raise ValueError(f"kv_cache shape {tuple(kv_cache.shape)} does not match qkv {tuple(qkv.shape)}")
+    return ropekv_dims(B, S, num_q_heads, num_kv_heads, D, cos_sin.shape[2], kv_cache.shape[3],
+                       cos_sin.shape[0], cos_sin.shape[1], style)
+
+
+# ------------------------------------------------------------ entry points --
+
+def rope_write_kv_packed(cos_sin: torch.Tensor, qkv: torch.Tensor, kv_cache: torch.Tensor,
+                         num_q_heads: int, num_kv_heads: int, style: int = NEOX,
+                         stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Empty cache: rotate Q and K of ``qkv`` in place and write K, V to slots 0..S-1.
+
+    cos_sin [csB, csS, r] float32; qkv [B, S, Hq+2Hkv, D] float16 (in/out);
+    kv_cache [B, 2, Hkv, cap, D] float16 (out).
+    """
+    dims = _contiguous_dims(cos_sin, qkv, kv_cache, num_q_heads, num_kv_heads, style)
+    dev = qkv.device
+    rc = load_library().rope_write_kv_packed(
+        _dev_ptr(cos_sin, "cos_sin", _F32, dev), _dev_ptr(qkv, "qkv", _F16, dev),
+        _dev_ptr(kv_cache, "kv_cache", _F16, dev), ctypes.byref(dims), _stream_handle(stream, dev))
+    _check_rc("rope_write_kv_packed", rc)
+
+
+def rope_write_kv_continuous(cos_sin: torch.Tensor, kv_cache_end_lens: torch.Tensor,
+                             qkv: torch.Tensor, kv_cache: torch.Tensor, q_out: torch.Tensor,
+                             num_q_heads: int, num_kv_heads: int, style: int = NEOX,
+                             stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Non-empty cache: token s of sequence b takes slot = position
+    kv_cache_end_lens[b] - S + s; rotated Q goes to ``q_out`` [B, S, Hq, D]."""
+    dims = _contiguous_dims(cos_sin, qkv, kv_cache, num_q_heads, num_kv_heads, style)
+    B, S, _, D = qkv.shape
+    if tuple(kv_cache_end_lens.shape) != (B,) or tuple(q_out.shape) != (B, S, num_q_heads, D):
+        raise ValueError("kv_cache_end_lens [B] and q_out [B,S,Hq,D] expected")
+    dev = qkv.device
+    rc = load_library().rope_write_kv_continuous(
+        _dev_ptr(cos_sin, "cos_sin", _F32, dev),
+        _dev_ptr(kv_cache_end_lens, "kv_cache_end_lens", _I32, dev),
+        _dev_ptr(qkv, "qkv", _F16, dev), _dev_ptr(kv_cache, "kv_cache", _F16, dev),
+        _dev_ptr(q_out, "q_out", _F16, dev), ctypes.byref(dims), _stream_handle(stream, dev))
+    _check_rc("rope_write_kv_continuous", rc)
+
+
+def rope_write_kv_tree(cos_sin: torch.Tensor, kv_cache_end_lens: torch.Tensor,
+                       token_pos_ids: torch.Tensor, qkv: torch.Tensor, kv_cache: torch.Tensor,
+                       q_out: torch.Tensor, num_q_heads: int, num_kv_heads: int,
+                       style: int = NEOX, stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Tree speculative decoding: RoPE position token_pos_ids[b, s], cache slot
+    kv_cache_end_lens[b] - S + s."""
+    dims = _contiguous_dims(cos_sin, qkv, kv_cache, num_q_heads, num_kv_heads, style)
+    B, S, _, D = qkv.shape
+    if tuple(kv_cache_end_lens.shape) != (B,) or tuple(token_pos_ids.shape) != (B, S) \
+            or tuple(q_out.shape) != (B, S, num_q_heads, D):
+        raise ValueError("kv_cache_end_lens [B], token_pos_ids [B,S], q_out [B,S,Hq,D] expected")
+    dev = qkv.device
+    rc = load_library().rope_write_kv_tree(
+        _dev_ptr(cos_sin, "cos_sin", _F32, dev),
+        _dev_ptr(kv_cache_end_lens, "kv_cache_end_lens", _I32, dev),
+        _dev_ptr(token_pos_ids, "token_pos_ids", _I32, dev),
+        _dev_ptr(qkv, "qkv", _F16, dev), _dev_ptr(kv_cache, "kv_cache", _F16, dev),
+        _dev_ptr(q_out, "q_out", _F16, dev), ctypes.byref(dims), _stream_handle(stream, dev))
+    _check_rc("rope_write_kv_tree", rc)
+
+
+def paged_kv_delta_update(k_delta: torch.Tensor, v_delta: torch.Tensor, kv_cache: torch.Tensor,
+                          token_aligned_cos_sin: torch.Tensor, delta_positions: torch.Tensor,
+                          delta_token_to_sequence: torch.Tensor, page_table: torch.Tensor,
+                          batch_size: Optional[int] = None, style: int = NEOX,
+                          stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Paged delta update. k_delta, v_delta [N, Hkv, D] float16;
+    kv_cache [2, numPages, tokensPerPage, Hkv, D] float16; token_aligned_cos_sin
+    [N, r] float32; delta_positions, delta_token_to_sequence [N] int32;
+    page_table [B, 2, maxPagesPerSeq] int32. batch_size defaults to B."""
+    if k_delta.dim() != 3 or kv_cache.dim() != 5 or page_table.dim() != 3 \
+            or token_aligned_cos_sin.dim() != 2:
+        raise ValueError("k_delta [N,Hkv,D], kv_cache [2,P,TPP,Hkv,D], page_table [B,2,M], "
+                         "token_aligned_cos_sin [N,r] expected")
+    N, Hkv, D = k_delta.shape
+    two, num_pages, tpp, hk2, d2 = kv_cache.shape
+    B, two_b, mpps = page_table.shape
+    if tuple(v_delta.shape) != (N, Hkv, D) or two != 2 or hk2 != Hkv or d2 != D or two_b != 2 \
+            or token_aligned_cos_sin.shape[0] != N or tuple(delta_positions.shape) != (N,) \
+            or tuple(delta_token_to_sequence.shape) != (N,):
+        raise ValueError("inconsistent shapes for paged_kv_delta_update")
+    if batch_size is None:
+        batch_size = B
+    if batch_size > B:
+        raise ValueError("batch_size exceeds the page table's rows")
+    dev = k_delta.device
+    rc = load_library().paged_kv_delta_update(
+        _dev_ptr(k_delta, "k_delta", _F16, dev), _dev_ptr(v_delta, "v_delta", _F16, dev),
+        _dev_ptr(kv_cache, "kv_cache", _F16, dev),
+        _dev_ptr(token_aligned_cos_sin, "token_aligned_cos_sin", _F32, dev),
+        _dev_ptr(delta_positions, "delta_positions", _I32, dev),
+        _dev_ptr(delta_token_to_sequence, "delta_token_to_sequence", _I32, dev),
+        _dev_ptr(page_table, "page_table", _I32, dev),
+        N, batch_size, Hkv, D, token_aligned_cos_sin.shape[1], num_pages, mpps, tpp, style,
+        _stream_handle(stream, dev))
+    _check_rc("paged_kv_delta_update", rc)

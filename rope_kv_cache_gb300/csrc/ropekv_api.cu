@@ -1,0 +1,333 @@
+// ropekv_api.cu -- the C ABI of libropekv.so: host-side argument checks, the
+// choice of kernel instantiation and launch shape, and one launch per call on
+// the caller's stream. Declarations and the meaning of every argument are in
+// include/ropekv.h. Nothing here allocates, synchronises or keeps state.
+#include <cuda_runtime.h>
+
+#include <stdint.h>
+
+#include "ropekv.h"
+#include "ropekv_kernels.cuh"
+
+namespace {
+
+using ropekv::PagedArgs;
+using ropekv::TokenArgs;
+
+constexpr int kMaxThreads = 256;
+
+bool aligned16(const void* p)
+{
+    return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+int check_head_dims(int32_t D, int32_t r)
+{
+    if (D != 64 && D != 128 && D != 256)
+        return ROPEKV_ERR_HEAD_DIM;
+    if (r < 16 || r > D || (r % 16) != 0)
+        return ROPEKV_ERR_ROTARY_DIM;
+    return ROPEKV_OK;
+}
+
+// Launch shape for `units` tokens (or rows) of `items` items each.
+// IPT = items per thread; CTAs per unit split a unit's items evenly over
+// blocks of at most 256 threads, rounded to whole warps (a warp size is a
+// multiple of every D/16, which keeps each thread on one item index).
+struct Shape {
+    int threads;
+    int ipt;
+    int ctasPerUnit;
+};
+
+Shape pick_shape(int items, long long units)
+{
+    Shape sh;
+    sh.ipt = (units >= 1024) ? 2 : 1;
+    sh.ctasPerUnit = (items + kMaxThreads * sh.ipt - 1) / (kMaxThreads * sh.ipt);
+    int per = (items + sh.ctasPerUnit * sh.ipt - 1) / (sh.ctasPerUnit * sh.ipt);
+    sh.threads = ((per + 31) / 32) * 32;
+    return sh;
+}
+
+template <int D, int STYLE, int MODE, int IPT>
+void launch_token(const TokenArgs& a, long long tokens, const Shape& sh, cudaStream_t st)
+{
+    const unsigned grid = (unsigned)(tokens * sh.ctasPerUnit);
+    ropekv::rope_kv_token_kernel<D, STYLE, MODE, IPT><<<grid, sh.threads, 0, st>>>(a);
+}
+
+template <int D, int STYLE, int MODE>
+void dispatch_ipt(const TokenArgs& a, long long tokens, const Shape& sh, cudaStream_t st)
+{
+    if (sh.ipt == 2)
+        launch_token<D, STYLE, MODE, 2>(a, tokens, sh, st);
+    else
+        launch_token<D, STYLE, MODE, 1>(a, tokens, sh, st);
+}
+
+template <int D, int MODE>
+void dispatch_style(const TokenArgs& a, int style, long long tokens, const Shape& sh,
+                    cudaStream_t st)
+{
+    if (style == ROPEKV_GPTJ)
+        dispatch_ipt<D, ropekv::kGptj, MODE>(a, tokens, sh, st);
+    else
+        dispatch_ipt<D, ropekv::kNeox, MODE>(a, tokens, sh, st);
+}
+
+template <int MODE>
+void dispatch_token(const TokenArgs& a, int D, int style, long long tokens, const Shape& sh,
+                    cudaStream_t st)
+{
+    switch (D) {
+    case 64: dispatch_style<64, MODE>(a, style, tokens, sh, st); break;
+    case 128: dispatch_style<128, MODE>(a, style, tokens, sh, st); break;
+    default: dispatch_style<256, MODE>(a, style, tokens, sh, st); break;
+    }
+}
+
+template <int D, int STYLE>
+void launch_paged(const PagedArgs& a, long long rows, const Shape& sh, cudaStream_t st)
+{
+    const unsigned grid = (unsigned)(rows * sh.ctasPerUnit);
+    if (sh.ipt == 2)
+        ropekv::paged_delta_kernel<D, STYLE, 2><<<grid, sh.threads, 0, st>>>(a);
+    else
+        ropekv::paged_delta_kernel<D, STYLE, 1><<<grid, sh.threads, 0, st>>>(a);
+}
+
+template <int D>
+void dispatch_paged_style(const PagedArgs& a, int style, long long rows, const Shape& sh,
+                          cudaStream_t st)
+{
+    if (style == ROPEKV_GPTJ)
+        launch_paged<D, ropekv::kGptj>(a, rows, sh, st);
+    else
+        launch_paged<D, ropekv::kNeox>(a, rows, sh, st);
+}
+
+int launch_status()
+{
+    return cudaGetLastError() == cudaSuccess ? ROPEKV_OK : ROPEKV_ERR_LAUNCH;
+}
+
+// Checks shared by the three contiguous-cache calls. On success fills the
+// kernel arguments that depend only on the sizes and returns the token count.
+int check_dims(const ropekv_dims* d, long long* tokens)
+{
+    if (d == nullptr)
+        return ROPEKV_ERR_NULL_POINTER;
+    if (d->style != ROPEKV_NEOX && d->style != ROPEKV_GPTJ)
+        return ROPEKV_ERR_STYLE;
+    int rc = check_head_dims(d->headDim, d->rotaryDim);
+    if (rc != ROPEKV_OK)
+        return rc;
+    if (d->numQHeads <= 0 || d->numKVHeads <= 0 || d->numQHeads % d->numKVHeads != 0)
+        return ROPEKV_ERR_HEADS;
+    if (d->batch < 0 || d->seqLen < 0 || d->kvCapacity < 0 || d->cosSinSeqLen < 0)
+        return ROPEKV_ERR_SHAPE;
+    if (d->cosSinBatch != 1 && d->cosSinBatch != d->batch)
+        return ROPEKV_ERR_COS_SIN_BATCH;
+    const long long H = (long long)d->numQHeads + 2LL * d->numKVHeads;
+    if (H * (d->headDim / 16) > (1LL << 30))
+        return ROPEKV_ERR_SHAPE;
+    *tokens = (long long)d->batch * d->seqLen;
+    return ROPEKV_OK;
+}
+
+TokenArgs token_args(const ropekv_dims* d)
+{
+    TokenArgs a = {};
+    a.S = d->seqLen;
+    a.Hq = d->numQHeads;
+    a.Hkv = d->numKVHeads;
+    a.r = d->rotaryDim;
+    a.cap = d->kvCapacity;
+    a.csBatch = d->cosSinBatch;
+    a.csSeq = d->cosSinSeqLen;
+    a.itemsPerToken = (d->numQHeads + 2 * d->numKVHeads) * (d->headDim / 16);
+    return a;
+}
+
+int launch_contiguous(TokenArgs a, const ropekv_dims* d, long long tokens, int mode,
+                      cudaStream_t st)
+{
+    const Shape sh = pick_shape(a.itemsPerToken, tokens);
+    if (tokens * sh.ctasPerUnit > 0x7FFFFFFFLL)
+        return ROPEKV_ERR_SHAPE;
+    a.ctasPerToken = sh.ctasPerUnit;
+    switch (mode) {
+    case ropekv::kPacked:
+        dispatch_token<ropekv::kPacked>(a, d->headDim, d->style, tokens, sh, st);
+        break;
+    case ropekv::kContinuous:
+        dispatch_token<ropekv::kContinuous>(a, d->headDim, d->style, tokens, sh, st);
+        break;
+    default:
+        dispatch_token<ropekv::kTree>(a, d->headDim, d->style, tokens, sh, st);
+        break;
+    }
+    return launch_status();
+}
+
+}  // namespace
+
+extern "C" {
+
+int rope_write_kv_packed(const float* cosSin, uint16_t* qkv, uint16_t* kvCache,
+                         const ropekv_dims* dims, void* stream)
+{
+    long long tokens = 0;
+    int rc = check_dims(dims, &tokens);
+    if (rc != ROPEKV_OK)
+        return rc;
+    if (dims->seqLen > dims->kvCapacity || dims->seqLen > dims->cosSinSeqLen)
+        return ROPEKV_ERR_CAPACITY;
+    if (tokens == 0)
+        return ROPEKV_OK;
+    if (!cosSin || !qkv || !kvCache)
+        return ROPEKV_ERR_NULL_POINTER;
+    if (!aligned16(cosSin) || !aligned16(qkv) || !aligned16(kvCache))
+        return ROPEKV_ERR_MISALIGNED;
+    TokenArgs a = token_args(dims);
+    a.cosSin = cosSin;
+    a.qkv = qkv;
+    a.qkvOut = qkv;
+    a.cache = kvCache;
+    return launch_contiguous(a, dims, tokens, ropekv::kPacked, (cudaStream_t)stream);
+}
+
+int rope_write_kv_continuous(const float* cosSin, const int32_t* kvCacheEndLens,
+                             const uint16_t* qkv, uint16_t* kvCache, uint16_t* qOut,
+                             const ropekv_dims* dims, void* stream)
+{
+    long long tokens = 0;
+    int rc = check_dims(dims, &tokens);
+    if (rc != ROPEKV_OK)
+        return rc;
+    if (tokens == 0)
+        return ROPEKV_OK;
+    if (!cosSin || !kvCacheEndLens || !qkv || !kvCache || !qOut)
+        return ROPEKV_ERR_NULL_POINTER;
+    if (!aligned16(cosSin) || !aligned16(kvCacheEndLens) || !aligned16(qkv) ||
+        !aligned16(kvCache) || !aligned16(qOut))
+        return ROPEKV_ERR_MISALIGNED;
+    TokenArgs a = token_args(dims);
+    a.cosSin = cosSin;
+    a.endLens = kvCacheEndLens;
+    a.qkv = qkv;
+    a.cache = kvCache;
+    a.qOut = qOut;
+    return launch_contiguous(a, dims, tokens, ropekv::kContinuous, (cudaStream_t)stream);
+}
+
+int rope_write_kv_tree(const float* cosSin, const int32_t* kvCacheEndLens,
+                       const int32_t* tokenPosIds, const uint16_t* qkv, uint16_t* kvCache,
+                       uint16_t* qOut, const ropekv_dims* dims, void* stream)
+{
+    long long tokens = 0;
+    int rc = check_dims(dims, &tokens);
+    if (rc != ROPEKV_OK)
+        return rc;
+    if (tokens == 0)
+        return ROPEKV_OK;
+    if (!cosSin || !kvCacheEndLens || !tokenPosIds || !qkv || !kvCache || !qOut)
+        return ROPEKV_ERR_NULL_POINTER;
+    if (!aligned16(cosSin) || !aligned16(kvCacheEndLens) || !aligned16(tokenPosIds) ||
+        !aligned16(qkv) || !aligned16(kvCache) || !aligned16(qOut))
+        return ROPEKV_ERR_MISALIGNED;
+    TokenArgs a = token_args(dims);
+    a.cosSin = cosSin;
+    a.endLens = kvCacheEndLens;
+    a.posIds = tokenPosIds;
+    a.qkv = qkv;
+    a.cache = kvCache;
+    a.qOut = qOut;
+    return launch_contiguous(a, dims, tokens, ropekv::kTree, (cudaStream_t)stream);
+}
+
+int paged_kv_delta_update(const uint16_t* kDelta, const uint16_t* vDelta, uint16_t* kvCache,
+                          const float* tokenAlignedCosSin, const int32_t* deltaPositions,
+                          const int32_t* deltaTokenToSequence, const int32_t* pageTable,
+                          int32_t numDeltaTokens, int32_t batchSize, int32_t numKVHeads,
+                          int32_t headDim, int32_t rotaryDim, int32_t numPages,
+                          int32_t maxPagesPerSeq, int32_t tokensPerPage, int32_t style,
+                          void* stream)
+{
+    if (style != ROPEKV_NEOX && style != ROPEKV_GPTJ)
+        return ROPEKV_ERR_STYLE;
+    int rc = check_head_dims(headDim, rotaryDim);
+    if (rc != ROPEKV_OK)
+        return rc;
+    if (numKVHeads <= 0)
+        return ROPEKV_ERR_HEADS;
+    if (numDeltaTokens < 0 || batchSize < 0 || numPages < 0 || maxPagesPerSeq < 0 ||
+        tokensPerPage <= 0)
+        return ROPEKV_ERR_SHAPE;
+    const long long items = 2LL * numKVHeads * (headDim / 16);
+    if (items > (1LL << 30))
+        return ROPEKV_ERR_SHAPE;
+    if (numDeltaTokens == 0)
+        return ROPEKV_OK;
+    if (!kDelta || !vDelta || !kvCache || !tokenAlignedCosSin || !deltaPositions ||
+        !deltaTokenToSequence || (!pageTable && batchSize > 0))
+        return ROPEKV_ERR_NULL_POINTER;
+    if (!aligned16(kDelta) || !aligned16(vDelta) || !aligned16(kvCache) ||
+        !aligned16(tokenAlignedCosSin) || !aligned16(deltaPositions) ||
+        !aligned16(deltaTokenToSequence) || !aligned16(pageTable))
+        return ROPEKV_ERR_MISALIGNED;
+    if (batchSize == 0)
+        return ROPEKV_OK;  // every row names a sequence >= batchSize: nothing to write
+    PagedArgs a = {};
+    a.kDelta = kDelta;
+    a.vDelta = vDelta;
+    a.pool = kvCache;
+    a.cosSin = tokenAlignedCosSin;
+    a.positions = deltaPositions;
+    a.seqIds = deltaTokenToSequence;
+    a.pageTable = pageTable;
+    a.B = batchSize;
+    a.Hkv = numKVHeads;
+    a.r = rotaryDim;
+    a.numPages = numPages;
+    a.mpps = maxPagesPerSeq;
+    a.tpp = tokensPerPage;
+    a.itemsPerRow = (int32_t)items;
+    const Shape sh = pick_shape(a.itemsPerRow, numDeltaTokens);
+    if ((long long)numDeltaTokens * sh.ctasPerUnit > 0x7FFFFFFFLL)
+        return ROPEKV_ERR_SHAPE;
+    a.ctasPerRow = sh.ctasPerUnit;
+    cudaStream_t st = (cudaStream_t)stream;
+    switch (headDim) {
+    case 64: dispatch_paged_style<64>(a, style, numDeltaTokens, sh, st); break;
+    case 128: dispatch_paged_style<128>(a, style, numDeltaTokens, sh, st); break;
+    default: dispatch_paged_style<256>(a, style, numDeltaTokens, sh, st); break;
+    }
+    return launch_status();
+}
+
+int rope_check_capacity(int32_t cosSinSeqLen, int32_t kvCapacity)
+{
+    return cosSinSeqLen > kvCapacity ? ROPEKV_ERR_CAPACITY : ROPEKV_OK;
+}
+
+const char* ropekv_status_string(int status)
+{
+    switch (status) {
+    case ROPEKV_OK: return "ok";
+    case ROPEKV_ERR_NULL_POINTER: return "a required pointer is NULL";
+    case ROPEKV_ERR_MISALIGNED: return "a tensor pointer is not 16-byte aligned";
+    case ROPEKV_ERR_HEAD_DIM: return "headDim must be 64, 128 or 256";
+    case ROPEKV_ERR_ROTARY_DIM: return "rotaryDim must be a multiple of 16 in [16, headDim]";
+    case ROPEKV_ERR_HEADS: return "head counts must be positive, numQHeads a multiple of numKVHeads";
+    case ROPEKV_ERR_SHAPE: return "a size is negative or too large";
+    case ROPEKV_ERR_COS_SIN_BATCH: return "cosSinBatch must be 1 or batch";
+    case ROPEKV_ERR_CAPACITY: return "capacity check failed";
+    case ROPEKV_ERR_STYLE: return "style must be ROPEKV_NEOX or ROPEKV_GPTJ";
+    case ROPEKV_ERR_LAUNCH: return "CUDA kernel launch failed";
+    default: return "unknown status";
+    }
+}
+
+}  // extern "C"

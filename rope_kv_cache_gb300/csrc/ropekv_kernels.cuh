@@ -1,0 +1,347 @@
+// ropekv_kernels.cuh -- sm_103a kernels of the fused RoPE + KV-cache write.
+//
+// What is computed (sources cited by page title and section):
+//   * x' = x*cos + rotate(x)*sin on the first rotaryDim dims of every Q and K
+//     head (sglang rope_cache.py: _unit_rope; rotate() layouts of
+//     _get_neox_rotated_x / _get_gptj_rotated_x; frequency index of kernel
+//     Stage 2.1 with the half-width cos/sin table read as in _load_cos_sin).
+//   * the contiguous-cache placement of TensorRT-Edge-LLM "Apply Rope Write KV"
+//     (packed in place / continuous / tree), and
+//   * the paged placement and skip rules of TensorRT-Edge-LLM "Dflash Runtime
+//     Kernels", launchDFlashTargetKVCacheUpdate.
+//
+// Work decomposition. A head of D FP16 values is D/8 16-byte vectors. An
+// "item" is two vectors of one head handled by one thread:
+//   rotated region (item i < r/16): vectors i and i + r/16. For NeoX these are
+//     partners (dims 8i+k and 8i+k+r/2 share frequency 8i+k), so the half swap
+//     happens inside the thread's registers; for GPT-J each vector holds four
+//     complete (2j, 2j+1) pairs, so the pair swap is inside one half2 word;
+//   pass-through region (i >= r/16): two vectors past rotaryDim, copied as bits.
+// V heads use the same vector pairs and are copied as bits. Items are numbered
+// head-major inside a token, a CTA covers a contiguous run of one token's items
+// and the block size is a multiple of D/16, so every thread keeps one item
+// index i for all its heads: it loads its 8 cos + 8 sin values once per token
+// and reuses them for every Q and K head it rotates. Loads are issued before
+// the position / cos/sin chain resolves so their latencies overlap.
+//
+// All loads and stores are 16-byte vectors; a warp touches whole 32-byte
+// sectors. Math is FP32 with round-to-nearest-even back to FP16. Invalid
+// device-side indices are skipped; nothing traps or waits.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace ropekv {
+
+enum Style : int { kNeox = 0, kGptj = 1 };
+enum Mode : int { kPacked = 0, kContinuous = 1, kTree = 2 };
+
+// Arguments of the contiguous-cache kernel (packed / continuous / tree).
+struct TokenArgs {
+    const float* cosSin;       // [csBatch, csSeq, r]
+    const int32_t* endLens;    // [B]      (continuous, tree)
+    const int32_t* posIds;     // [B, S]   (tree)
+    const uint16_t* qkv;       // [B, S, Hq + 2 Hkv, D]
+    uint16_t* qkvOut;          // same buffer as qkv for the packed in-place call
+    uint16_t* cache;           // [B, 2, Hkv, cap, D]
+    uint16_t* qOut;            // [B, S, Hq, D] (continuous, tree)
+    int32_t S, Hq, Hkv, r, cap, csBatch, csSeq;
+    int32_t itemsPerToken;     // (Hq + 2 Hkv) * D / 16
+    int32_t ctasPerToken;      // CTAs sharing one token's items
+};
+
+// Arguments of the paged delta kernel.
+struct PagedArgs {
+    const uint16_t* kDelta;    // [N, Hkv, D]
+    const uint16_t* vDelta;    // [N, Hkv, D]
+    uint16_t* pool;            // [2, numPages, tpp, Hkv, D]
+    const float* cosSin;       // [N, r] token-aligned
+    const int32_t* positions;  // [N]
+    const int32_t* seqIds;     // [N]
+    const int32_t* pageTable;  // [B, 2, mpps]
+    int32_t B, Hkv, r, numPages, mpps, tpp;
+    int32_t itemsPerRow;       // 2 * Hkv * D / 16 (K heads, then V heads)
+    int32_t ctasPerRow;
+};
+
+// --------------------------------------------------------------- helpers --
+
+__device__ __forceinline__ uint4 load_ro(const uint16_t* p)
+{
+    return __ldg(reinterpret_cast<const uint4*>(p));
+}
+
+__device__ __forceinline__ uint4 load_rw(const uint16_t* p)
+{
+    return *reinterpret_cast<const uint4*>(p);
+}
+
+__device__ __forceinline__ void store_v(uint16_t* p, const uint4& v)
+{
+    *reinterpret_cast<uint4*>(p) = v;
+}
+
+__device__ __forceinline__ float4 load_f4(const float* p)
+{
+    return __ldg(reinterpret_cast<const float4*>(p));
+}
+
+__device__ __forceinline__ __half2& h2(uint32_t& w)
+{
+    return *reinterpret_cast<__half2*>(&w);
+}
+
+// The two vectors of item i (in units of 16-byte vectors inside a head).
+template <int D>
+__device__ __forceinline__ void item_vectors(int i, int r, int& va, int& vb)
+{
+    const int rot_items = r >> 4;
+    if (i < rot_items) {
+        va = i;
+        vb = i + rot_items;
+    } else {
+        const int j = i - rot_items;
+        va = (r >> 3) + j;
+        vb = va + ((D - r) >> 4);
+    }
+}
+
+// cos/sin of the frequencies item i uses, from one table row of r floats.
+// NeoX: frequencies 8i..8i+7 (shared by both vectors).
+// GPT-J: frequencies 4i..4i+3 (first vector) and r/4 + 4i .. +3 (second).
+template <int STYLE>
+__device__ __forceinline__ void load_cos_sin(const float* row, int i, int r, float c[8],
+                                             float s[8])
+{
+    const int h = r >> 1;
+    float4 a, b, e, f;
+    if (STYLE == kNeox) {
+        a = load_f4(row + 8 * i);
+        b = load_f4(row + 8 * i + 4);
+        e = load_f4(row + h + 8 * i);
+        f = load_f4(row + h + 8 * i + 4);
+    } else {
+        a = load_f4(row + 4 * i);
+        b = load_f4(row + 4 * i + (r >> 2));
+        e = load_f4(row + h + 4 * i);
+        f = load_f4(row + h + 4 * i + (r >> 2));
+    }
+    c[0] = a.x; c[1] = a.y; c[2] = a.z; c[3] = a.w;
+    c[4] = b.x; c[5] = b.y; c[6] = b.z; c[7] = b.w;
+    s[0] = e.x; s[1] = e.y; s[2] = e.z; s[3] = e.w;
+    s[4] = f.x; s[5] = f.y; s[6] = f.z; s[7] = f.w;
+}
+
+// NeoX: va holds dims 8i..8i+7 (first half), vb the partner dims 8i+r/2...;
+// a' = a*c - b*s, b' = b*c + a*s with the frequency of the pair.
+__device__ __forceinline__ void rotate_neox(uint4& va, uint4& vb, const float c[8],
+                                            const float s[8])
+{
+    uint32_t* wa = reinterpret_cast<uint32_t*>(&va);
+    uint32_t* wb = reinterpret_cast<uint32_t*>(&vb);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float2 a = __half22float2(h2(wa[k]));
+        const float2 b = __half22float2(h2(wb[k]));
+        const float c0 = c[2 * k], c1 = c[2 * k + 1];
+        const float s0 = s[2 * k], s1 = s[2 * k + 1];
+        const float ax = fmaf(a.x, c0, -(b.x * s0));
+        const float ay = fmaf(a.y, c1, -(b.y * s1));
+        const float bx = fmaf(b.x, c0, a.x * s0);
+        const float by = fmaf(b.y, c1, a.y * s1);
+        h2(wa[k]) = __floats2half2_rn(ax, ay);
+        h2(wb[k]) = __floats2half2_rn(bx, by);
+    }
+}
+
+// GPT-J: each half2 word is one (2j, 2j+1) pair; word k of the vector uses
+// frequency c[k] / s[k].
+__device__ __forceinline__ void rotate_gptj(uint4& v, const float* c, const float* s)
+{
+    uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float2 x = __half22float2(h2(w[k]));
+        const float e = fmaf(x.x, c[k], -(x.y * s[k]));
+        const float o = fmaf(x.y, c[k], x.x * s[k]);
+        h2(w[k]) = __floats2half2_rn(e, o);
+    }
+}
+
+template <int STYLE>
+__device__ __forceinline__ void rotate_item(uint4& va, uint4& vb, const float c[8],
+                                            const float s[8])
+{
+    if (STYLE == kNeox) {
+        rotate_neox(va, vb, c, s);
+    } else {
+        rotate_gptj(va, c, s);
+        rotate_gptj(vb, c + 4, s + 4);
+    }
+}
+
+// ------------------------------------------------- contiguous-cache kernel --
+//
+// Grid: tokens * ctasPerToken CTAs; CTA (token, part) covers items
+// [part * blockDim * IPT, (part + 1) * blockDim * IPT) of the token, each thread
+// items tid + k * blockDim for k < IPT. blockDim is a multiple of D/16.
+template <int D, int STYLE, int MODE, int IPT>
+__global__ void __launch_bounds__(256) rope_kv_token_kernel(const TokenArgs a)
+{
+    constexpr int kItemsPerHead = D / 16;
+    const int tok = blockIdx.x / a.ctasPerToken;
+    const int part = blockIdx.x - tok * a.ctasPerToken;
+    const int b = tok / a.S;
+    const int s = tok - b * a.S;
+    const int H = a.Hq + 2 * a.Hkv;
+    const int i = threadIdx.x % kItemsPerHead;
+    const int item0 = part * blockDim.x * IPT + threadIdx.x;
+
+    int va, vb;
+    item_vectors<D>(i, a.r, va, vb);
+
+    // 1. this thread's QKV vectors (independent of the position chain)
+    const uint16_t* tokIn = a.qkv + (size_t)tok * H * D;
+    uint4 xa[IPT], xb[IPT];
+#pragma unroll
+    for (int k = 0; k < IPT; ++k) {
+        const int item = item0 + k * blockDim.x;
+        if (item < a.itemsPerToken) {
+            const int head = item / kItemsPerHead;
+            const uint16_t* p = tokIn + (size_t)head * D;
+            if (MODE == kPacked) {
+                xa[k] = load_rw(p + 8 * va);
+                xb[k] = load_rw(p + 8 * vb);
+            } else {
+                xa[k] = load_ro(p + 8 * va);
+                xb[k] = load_ro(p + 8 * vb);
+            }
+        }
+    }
+
+    // 2. position (cos/sin row) and cache slot of the token
+    int pos, slot;
+    if (MODE == kPacked) {
+        pos = s;
+        slot = s;
+    } else {
+        slot = __ldg(a.endLens + b) - a.S + s;
+        pos = (MODE == kTree) ? __ldg(a.posIds + tok) : slot;
+        if (slot < 0 || slot >= a.cap || pos < 0 || pos >= a.csSeq)
+            return;  // skipped token: nothing written
+    }
+
+    // 3. cos/sin for this thread's frequencies
+    float c[8], sn[8];
+    const bool rotItem = i < (a.r >> 4);
+    if (rotItem) {
+        const int bc = (a.csBatch == 1) ? 0 : b;
+        const float* row = a.cosSin + ((size_t)bc * a.csSeq + pos) * a.r;
+        load_cos_sin<STYLE>(row, i, a.r, c, sn);
+    }
+
+    // 4. rotate and store
+#pragma unroll
+    for (int k = 0; k < IPT; ++k) {
+        const int item = item0 + k * blockDim.x;
+        if (item >= a.itemsPerToken)
+            continue;
+        const int head = item / kItemsPerHead;
+        uint16_t* dst;
+        if (head < a.Hq + a.Hkv) {
+            if (rotItem)
+                rotate_item<STYLE>(xa[k], xb[k], c, sn);
+            if (head < a.Hq) {
+                dst = (MODE == kPacked) ? a.qkvOut + (size_t)tok * H * D + (size_t)head * D
+                                        : a.qOut + ((size_t)tok * a.Hq + head) * D;
+            } else {
+                const int hk = head - a.Hq;
+                if (MODE == kPacked) {
+                    uint16_t* q = a.qkvOut + (size_t)tok * H * D + (size_t)head * D;
+                    store_v(q + 8 * va, xa[k]);
+                    store_v(q + 8 * vb, xb[k]);
+                }
+                dst = a.cache + ((((size_t)b * 2 + 0) * a.Hkv + hk) * a.cap + slot) * D;
+            }
+        } else {
+            const int hv = head - a.Hq - a.Hkv;
+            dst = a.cache + ((((size_t)b * 2 + 1) * a.Hkv + hv) * a.cap + slot) * D;
+        }
+        store_v(dst + 8 * va, xa[k]);
+        store_v(dst + 8 * vb, xb[k]);
+    }
+}
+
+// --------------------------------------------------------- paged kernel --
+//
+// Grid: rows * ctasPerRow CTAs; items [0, Hkv*D/16) are K heads, the rest V
+// heads, split across the CTAs of a row like the token kernel.
+template <int D, int STYLE, int IPT>
+__global__ void __launch_bounds__(256) paged_delta_kernel(const PagedArgs a)
+{
+    constexpr int kItemsPerHead = D / 16;
+    const int t = blockIdx.x / a.ctasPerRow;
+    const int part = blockIdx.x - t * a.ctasPerRow;
+    const int i = threadIdx.x % kItemsPerHead;
+    const int item0 = part * blockDim.x * IPT + threadIdx.x;
+    const int kItems = a.Hkv * kItemsPerHead;
+
+    const int pos = __ldg(a.positions + t);
+    const int seq = __ldg(a.seqIds + t);
+    if (pos < 0 || seq < 0 || seq >= a.B)
+        return;  // padding row
+    const int lp = pos / a.tpp;
+    if (lp >= a.mpps)
+        return;  // past the sequence's logical pages
+    const int inPage = pos - lp * a.tpp;
+
+    int va, vb;
+    item_vectors<D>(i, a.r, va, vb);
+
+    // delta rows (issued before the page-table lookups resolve)
+    const size_t rowOff = (size_t)t * a.Hkv * D;
+    uint4 xa[IPT], xb[IPT];
+#pragma unroll
+    for (int k = 0; k < IPT; ++k) {
+        const int item = item0 + k * blockDim.x;
+        if (item < a.itemsPerRow) {
+            const bool isK = item < kItems;
+            const int head = (isK ? item : item - kItems) / kItemsPerHead;
+            const uint16_t* p = (isK ? a.kDelta : a.vDelta) + rowOff + (size_t)head * D;
+            xa[k] = load_ro(p + 8 * va);
+            xb[k] = load_ro(p + 8 * vb);
+        }
+    }
+
+    const int32_t* pt = a.pageTable + (size_t)seq * 2 * a.mpps + lp;
+    const int idK = __ldg(pt);
+    const int idV = __ldg(pt + a.mpps);
+    const bool kOk = idK >= 0 && idK < a.numPages;
+    const bool vOk = idV >= a.numPages && (int64_t)idV < 2 * (int64_t)a.numPages;
+
+    float c[8], sn[8];
+    const bool rotItem = i < (a.r >> 4);
+    if (rotItem && kOk)
+        load_cos_sin<STYLE>(a.cosSin + (size_t)t * a.r, i, a.r, c, sn);
+
+    const size_t rowElems = (size_t)a.Hkv * D;
+#pragma unroll
+    for (int k = 0; k < IPT; ++k) {
+        const int item = item0 + k * blockDim.x;
+        if (item >= a.itemsPerRow)
+            continue;
+        const bool isK = item < kItems;
+        if (isK ? !kOk : !vOk)
+            continue;
+        const int head = (isK ? item : item - kItems) / kItemsPerHead;
+        if (isK && rotItem)
+            rotate_item<STYLE>(xa[k], xb[k], c, sn);
+        const int id = isK ? idK : idV;  // flat page index of the [2, numPages] pool
+        uint16_t* dst = a.pool + ((size_t)id * a.tpp + inPage) * rowElems + (size_t)head * D;
+        store_v(dst + 8 * va, xa[k]);
+        store_v(dst + 8 * vb, xb[k]);
+    }
+}
+
+}  // namespace ropekv

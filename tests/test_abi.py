@@ -1,0 +1,136 @@
+"""The C-ABI library loads, exports every declared symbol and validates its
+arguments on the host (no GPU: only calls that must be rejected before any
+CUDA call, or that have nothing to do, are made)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import rope_kv_cache_gb300 as rk
+from rope_kv_cache_gb300 import build
+from rope_kv_cache_gb300._binding import ropekv_dims
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ropekv.h")
+
+A = ctypes.c_void_p(0x10000)        # a 16-byte aligned fake device address
+MIS = ctypes.c_void_p(0x10008)      # misaligned
+NUL = ctypes.c_void_p(0)
+
+OK = 0
+ERR = {n: -i for i, n in enumerate(
+    ["", "NULL", "MISALIGNED", "HEAD_DIM", "ROTARY_DIM", "HEADS", "SHAPE", "COS_SIN_BATCH",
+     "CAPACITY", "STYLE", "LAUNCH"])}
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build_library()
+    return rk.load_library()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return re.findall(r"ROPEKV_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
+
+
+def test_header_declares_the_entry_points():
+    names = set(declared_symbols())
+    assert names == {"rope_write_kv_packed", "rope_write_kv_continuous", "rope_write_kv_tree",
+                     "paged_kv_delta_update", "rope_check_capacity", "ropekv_status_string"}
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+
+
+def _dims(**kw):
+    d = dict(batch=2, seqLen=4, numQHeads=8, numKVHeads=2, headDim=128, rotaryDim=128,
+             kvCapacity=16, cosSinBatch=1, cosSinSeqLen=16, style=0)
+    d.update(kw)
+    return ropekv_dims(**d)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(headDim=96, rotaryDim=96), "HEAD_DIM"),
+    (dict(headDim=32, rotaryDim=32), "HEAD_DIM"),
+    (dict(rotaryDim=8), "ROTARY_DIM"),
+    (dict(rotaryDim=72), "ROTARY_DIM"),
+    (dict(rotaryDim=144), "ROTARY_DIM"),
+    (dict(rotaryDim=0), "ROTARY_DIM"),
+    (dict(numQHeads=6, numKVHeads=4), "HEADS"),
+    (dict(numKVHeads=0), "HEADS"),
+    (dict(batch=-1), "SHAPE"),
+    (dict(seqLen=-3), "SHAPE"),
+    (dict(cosSinBatch=3), "COS_SIN_BATCH"),
+    (dict(style=2), "STYLE"),
+])
+def test_contiguous_rejects_bad_sizes(lib, kw, want):
+    d = _dims(**kw)
+    assert lib.rope_write_kv_continuous(A, A, A, A, A, ctypes.byref(d), NUL) == ERR[want]
+    assert lib.rope_write_kv_tree(A, A, A, A, A, A, ctypes.byref(d), NUL) == ERR[want]
+    assert lib.rope_write_kv_packed(A, A, A, ctypes.byref(d), NUL) == ERR[want]
+
+
+def test_null_and_misaligned_pointers(lib):
+    d = _dims()
+    assert lib.rope_write_kv_continuous(A, NUL, A, A, A, ctypes.byref(d), NUL) == ERR["NULL"]
+    assert lib.rope_write_kv_continuous(A, A, A, A, MIS, ctypes.byref(d), NUL) == ERR["MISALIGNED"]
+    assert lib.rope_write_kv_tree(A, A, NUL, A, A, A, ctypes.byref(d), NUL) == ERR["NULL"]
+    assert lib.rope_write_kv_tree(A, A, MIS, A, A, A, ctypes.byref(d), NUL) == ERR["MISALIGNED"]
+    assert lib.rope_write_kv_packed(A, NUL, A, ctypes.byref(d), NUL) == ERR["NULL"]
+    assert lib.rope_write_kv_packed(MIS, A, A, ctypes.byref(d), NUL) == ERR["MISALIGNED"]
+    assert lib.rope_write_kv_packed(A, A, A, None, NUL) == ERR["NULL"]
+
+
+def test_packed_capacity_checks(lib):
+    assert lib.rope_write_kv_packed(A, A, A, ctypes.byref(_dims(seqLen=17)), NUL) == ERR["CAPACITY"]
+    d = _dims(seqLen=8, cosSinSeqLen=7)
+    assert lib.rope_write_kv_packed(A, A, A, ctypes.byref(d), NUL) == ERR["CAPACITY"]
+
+
+def test_empty_calls_launch_nothing(lib):
+    # zero tokens: OK without touching a pointer (NULLs allowed)
+    for d in (_dims(batch=0), _dims(seqLen=0)):
+        assert lib.rope_write_kv_continuous(NUL, NUL, NUL, NUL, NUL, ctypes.byref(d), NUL) == OK
+        assert lib.rope_write_kv_tree(NUL, NUL, NUL, NUL, NUL, NUL, ctypes.byref(d), NUL) == OK
+        assert lib.rope_write_kv_packed(NUL, NUL, NUL, ctypes.byref(d), NUL) == OK
+    assert lib.paged_kv_delta_update(NUL, NUL, NUL, NUL, NUL, NUL, NUL, 0, 4, 8, 128, 128, 16,
+                                     8, 64, 0, NUL) == OK
+
+
+def _paged(lib, *, ptrs=None, N=16, B=4, Hkv=8, D=128, r=128, P=16, M=8, tpp=64, style=0):
+    p = ptrs or [A] * 7
+    return lib.paged_kv_delta_update(*p, N, B, Hkv, D, r, P, M, tpp, style, NUL)
+
+
+def test_paged_rejects_bad_arguments(lib):
+    assert _paged(lib, D=80, r=80) == ERR["HEAD_DIM"]
+    assert _paged(lib, r=24) == ERR["ROTARY_DIM"]
+    assert _paged(lib, Hkv=0) == ERR["HEADS"]
+    assert _paged(lib, tpp=0) == ERR["SHAPE"]
+    assert _paged(lib, N=-1) == ERR["SHAPE"]
+    assert _paged(lib, P=-2) == ERR["SHAPE"]
+    assert _paged(lib, style=5) == ERR["STYLE"]
+    assert _paged(lib, ptrs=[A, A, NUL, A, A, A, A]) == ERR["NULL"]
+    assert _paged(lib, ptrs=[A, A, A, MIS, A, A, A]) == ERR["MISALIGNED"]
+    # batchSize 0: every row names a sequence >= batchSize, nothing to launch
+    assert _paged(lib, B=0) == OK
+
+
+def test_capacity_check(lib):
+    assert lib.rope_check_capacity(4096, 4096) == OK
+    assert lib.rope_check_capacity(100, 4096) == OK
+    assert lib.rope_check_capacity(4097, 4096) == ERR["CAPACITY"]
+    with pytest.raises(rk.RopeKVError):
+        rk.rope_check_capacity(9000, 8192)
+    rk.rope_check_capacity(8192, 8192)
+
+
+def test_status_strings(lib):
+    for code in range(0, -11, -1):
+        s = rk.ropekv_status_string(code)
+        assert s and s != "unknown status"
+    assert rk.ropekv_status_string(-99) == "unknown status"

@@ -1,0 +1,177 @@
+"""GPU parity of the contiguous-cache entry points against the oracle.
+
+Small seeded cases (several tiles, ragged tails, every head dim, partial
+rotary, MHA/GQA/MQA, skipped tokens, per-sequence tables) are compared on every
+output element. The benchmark workloads run at full size in the launch shape
+the benchmark times: packed_tiny and prefill on every element; decode and tree
+on every written slot plus a device-side count proving nothing else changed.
+"""
+import numpy as np
+import pytest
+
+import workloads
+from parity import (cache_rotated, check_contiguous, compare, qout_rotated, to_dev,
+                    to_host_bits)
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+NEOX, GPTJ = workloads.NEOX, workloads.GPTJ
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    from rope_kv_cache_gb300 import build
+    build.build_library()
+
+
+SMALL = [
+    # mode, style, D, r, Hq, Hkv, B, S, cap
+    ("continuous", NEOX, 128, 128, 8, 2, 3, 37, 128),
+    ("continuous", GPTJ, 128, 64, 4, 4, 2, 19, 64),
+    ("continuous", NEOX, 64, 32, 6, 3, 2, 50, 96),
+    ("continuous", NEOX, 256, 256, 8, 1, 2, 9, 40),
+    ("continuous", GPTJ, 256, 128, 16, 8, 1, 33, 64),
+    ("continuous", NEOX, 128, 16, 4, 2, 2, 5, 8),
+    ("continuous", NEOX, 64, 64, 4, 1, 2, 700, 1024),   # >= 1024 tokens: two items per thread
+    ("continuous", GPTJ, 128, 128, 64, 64, 1, 3, 8),    # 192 heads: several CTAs per token
+    ("tree", NEOX, 128, 128, 32, 8, 3, 20, 64),
+    ("tree", GPTJ, 64, 64, 4, 2, 4, 11, 32),
+    ("tree", GPTJ, 128, 64, 32, 8, 2, 64, 256),
+    ("packed", NEOX, 128, 128, 8, 2, 2, 40, 64),
+    ("packed", GPTJ, 64, 48, 4, 1, 1, 7, 8),
+    ("packed", NEOX, 256, 96, 4, 2, 3, 13, 13),
+    ("packed", GPTJ, 128, 128, 32, 8, 1, 1100, 1100),
+]
+
+
+def _small_case(mode, style, D, r, Hq, Hkv, B, S, cap, seed, cs_batch=1):
+    theta = 1e4 if style == GPTJ else 5e5
+    if mode == "continuous":
+        return workloads.make_continuous(B, S, Hq, Hkv, D, r, cap, style, theta, seed,
+                                         cs_batch=cs_batch, name=f"cont{seed}")
+    if mode == "tree":
+        return workloads.make_tree(B, S, Hq, Hkv, D, r, cap, style, theta, seed,
+                                   base_range=(0, cap - S), cs_batch=cs_batch, name=f"tree{seed}")
+    return workloads.make_packed(B, S, Hq, Hkv, D, r, cap, style, theta, seed, cs_batch=cs_batch,
+                                 cache_init="sentinel", name=f"packed{seed}")
+
+
+@pytest.mark.parametrize("idx", range(len(SMALL)))
+def test_small_cases(idx):
+    case = _small_case(*SMALL[idx], seed=100 + idx)
+    check_contiguous(case)
+
+
+@pytest.mark.parametrize("mode", ["continuous", "tree", "packed"])
+def test_per_sequence_tables(mode):
+    case = _small_case(mode, NEOX, 128, 128, 8, 2, 3, 17, 64, seed=7, cs_batch=3)
+    check_contiguous(case)
+
+
+def test_skipped_tokens_continuous():
+    # slots below 0, at/after the capacity, and past a short table are skipped
+    B, S, Hq, Hkv, D, r, cap = 4, 6, 4, 2, 128, 128, 32
+    case = workloads.make_continuous(B, S, Hq, Hkv, D, r, cap, NEOX, 5e5, seed=21,
+                                     end_lens=[3, 35, 32, 20], cs_seq=30, name="skips")
+    check_contiguous(case)
+
+
+def test_skipped_tokens_tree():
+    case = workloads.make_tree(3, 16, 8, 2, 128, 64, 64, GPTJ, 1e4, seed=22, base_range=(0, 40),
+                               cs_seq=44, name="tree_skips")
+    case.pos_ids[0, 3] = -1
+    case.pos_ids[1, 5] = -7
+    case.pos_ids[2, 0] = 44          # == cosSinSeqLen: skipped
+    case.end_lens[2] = 70            # last slots past the capacity
+    check_contiguous(case)
+
+
+def test_empty_inputs_are_no_ops():
+    import rope_kv_cache_gb300 as rk
+    for B, S in ((0, 5), (3, 0)):
+        case = workloads.make_continuous(B, S, 4, 2, 64, 64, 16, NEOX, 1e4, seed=3,
+                                         end_lens=np.full(B, S, dtype=np.int32))
+        cache = to_dev(case.new_cache())
+        qout = to_dev(case.new_qout())
+        rk.rope_write_kv_continuous(to_dev(case.cos_sin), to_dev(case.end_lens), to_dev(case.qkv),
+                                    cache, qout, 4, 2, NEOX)
+        torch.cuda.synchronize()
+        assert np.all(to_host_bits(cache) == workloads.SENTINEL)
+
+
+def test_non_default_stream_and_repeat():
+    case = _small_case("continuous", NEOX, 128, 128, 8, 2, 2, 33, 64, seed=5)
+    s = torch.cuda.Stream()
+    first = check_contiguous(case, stream=s)
+    second = check_contiguous(case, stream=s)
+    assert first == second
+
+
+# ---------------------------------------------------------- full configs --
+
+def test_config_packed_tiny():
+    case = workloads.config("packed_tiny")
+    check_contiguous(case)
+
+
+def test_config_prefill_full():
+    case = workloads.config("prefill")
+    stats = check_contiguous(case)
+    assert stats["qout"]["max_ulp"] <= 1 and stats["cache"]["max_ulp"] <= 1
+
+
+def _count_not_sentinel(cache_t) -> int:
+    n = 0
+    v = cache_t.view(torch.int16)
+    sent = np.uint16(workloads.SENTINEL).view(np.int16).item()
+    for b in range(v.shape[0]):
+        n += int((v[b] != sent).sum().item())
+    return n
+
+
+def _per_sequence_oracle(case, b):
+    """Oracle for sequence b alone (sequences are independent)."""
+    import oracle
+    sub_qkv = np.ascontiguousarray(case.qkv[b:b + 1])
+    cs = case.cos_sin if case.cos_sin.shape[0] == 1 else np.ascontiguousarray(case.cos_sin[b:b + 1])
+    cache = workloads.sentinel_fill((1, 2, case.Hkv, case.cap, case.D))
+    qout = workloads.sentinel_fill((1, case.S, case.Hq, case.D))
+    end = np.ascontiguousarray(case.end_lens[b:b + 1])
+    if case.mode == "tree":
+        oracle.tree(cs, end, np.ascontiguousarray(case.pos_ids[b:b + 1]), sub_qkv, cache, qout,
+                    case.Hq, case.Hkv, case.style)
+    else:
+        oracle.continuous(cs, end, sub_qkv, cache, qout, case.Hq, case.Hkv, case.style)
+    return cache[0], qout[0]
+
+
+@pytest.mark.parametrize("name", ["decode", "tree"])
+def test_config_written_slots_and_untouched(name):
+    import rope_kv_cache_gb300 as rk
+    case = workloads.config(name)
+    cs = to_dev(case.cos_sin)
+    qkv = to_dev(case.qkv)
+    end = to_dev(case.end_lens)
+    cache = to_dev(case.new_cache())
+    qout = to_dev(case.new_qout())
+    if case.mode == "tree":
+        rk.rope_write_kv_tree(cs, end, to_dev(case.pos_ids), qkv, cache, qout, case.Hq, case.Hkv,
+                              case.style)
+    else:
+        rk.rope_write_kv_continuous(cs, end, qkv, cache, qout, case.Hq, case.Hkv, case.style)
+    torch.cuda.synchronize()
+    g_qout = to_host_bits(qout)
+    written = 0
+    for b in range(case.B):
+        o_cache, o_qout = _per_sequence_oracle(case, b)
+        compare(g_qout[b], o_qout, qout_rotated((1,) + o_qout.shape, case.r)[0], f"{name} qOut b={b}")
+        slots = np.arange(case.S) + int(case.end_lens[b]) - case.S
+        slots = slots[(slots >= 0) & (slots < case.cap)]
+        g_rows = to_host_bits(cache[b][:, :, torch.as_tensor(slots, device=cache.device), :])
+        o_rows = np.ascontiguousarray(o_cache[:, :, slots, :])
+        compare(g_rows, o_rows, cache_rotated((1,) + o_rows.shape, case.r)[0], f"{name} cache b={b}")
+        written += len(slots) * 2 * case.Hkv * case.D
+    assert _count_not_sentinel(cache) == written

@@ -336,3 +336,44 @@ def config(name: str):
         return make_paged(16384, 128, 8, 128, 128, 64, 512, 65536, NEOX, 5e5, seed=4,
                           valid_rows=15565, name=name)
     raise KeyError(name)
+
+
+# ----------------------------------------------- per-step input variants --
+
+def step_variant(case, k: int):
+    """Index inputs of step k of a benchmark ring, drawn from the same
+    distribution as the case's own (seed 1000 + k); step 0 is the case itself.
+
+    Contiguous cases: (end_lens, pos_ids) -- new per-sequence start/end offsets
+    (and tree bases) so every step writes different cache slots. Paged cases:
+    page_table -- fresh page permutations with the same unmapped fraction, so
+    every step writes different pages.
+    """
+    if k == 0:
+        if isinstance(case, PagedCase):
+            return case.page_table
+        return case.end_lens, case.pos_ids
+    rng = rng_for(1000 + k)
+    if isinstance(case, PagedCase):
+        t = case.page_table.copy()
+        B, _, M = t.shape
+        n = B * M
+        reps = -(-n // case.num_pages)
+        kp = np.concatenate([rng.permutation(case.num_pages) for _ in range(reps)])[:n]
+        vp = np.concatenate([rng.permutation(case.num_pages) for _ in range(reps)])[:n]
+        t[:, 0, :] = kp.reshape(B, M)
+        t[:, 1, :] = (vp + case.num_pages).reshape(B, M)
+        unmapped = case.page_table < 0
+        t[unmapped] = -1
+        return np.ascontiguousarray(t)
+    if case.mode == "packed":
+        return None, None
+    if case.mode == "tree":
+        depth = case.pos_ids - (case.end_lens - case.S)[:, None]
+        lo = int(case.end_lens.min() - case.S)
+        hi = int(case.end_lens.max() - case.S)
+        base = rng.integers(lo, hi + 1, size=case.B).astype(np.int32)
+        return (base + case.S).astype(np.int32), np.ascontiguousarray((base[:, None] + depth).astype(np.int32))
+    lo = int(case.end_lens.min())
+    hi = int(case.end_lens.max())
+    return rng.integers(lo, hi + 1, size=case.B).astype(np.int32), None
