@@ -1,0 +1,543 @@
+"""Benchmark of the fused RoPE + KV-cache write on GB300.
+
+One step = one call of the entry point over one batch of the workload (one
+kernel launch). The headline workload is the Llama-3-8B-shaped prefill
+(B=4, S=2048, Hq=32, Hkv=8, D=r=128, NeoX, continuous cache of 8192 slots);
+decode, tree, paged and the tiny packed case are measured in the same run and
+reported under "workloads".
+
+Timing: W untimed warm-up steps, then exactly K steps replayed from CUDA
+graphs, bracketed by a barrier and torch.cuda.synchronize(); CUDA events on the
+launching stream. Consecutive steps cycle through a ring of distinct input sets
+(and distinct cache slots / pages) whose footprint exceeds twice the L2 size,
+so no step reads what the previous one left in L2.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+For N > 1 (torchrun) every rank runs its own replica of the workload on its
+GPU (the path has no exchange step: weak scaling, no collective on the data
+path); value is the whole-job rate over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "fused RoPE+KV-write tokens/s and effective HBM GB/s (% of GB300 peak)"
+HEADLINE = "prefill"
+EXTRA = ("decode", "tree", "paged", "packed_tiny")
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+DESCR = {
+    "packed_tiny": "packed in-place, empty cache: B=1 S=16 Hq=4 Hkv=2 D=r=64 NeoX theta=1e4",
+    "prefill": "Llama-3-8B-shaped prefill, continuous cache: B=4 S=2048 Hq=32 Hkv=8 D=r=128 "
+               "NeoX theta=5e5, capacity 8192, start in [0,4096]",
+    "decode": "decode, continuous cache: B=256 S=1 Hq=32 Hkv=8 D=r=128 NeoX theta=5e5, "
+              "cache [256,2,8,8192,128], end lengths in [1,8192]",
+    "tree": "tree speculative decoding: B=64 S=64 Hq=32 Hkv=8 D=128 r=64 GPT-J theta=1e4, "
+            "depth 0..6, base in [128,4000], capacity 4096",
+    "paged": "paged delta update: 16384 rows (15565 valid) over B=128, Hkv=8 D=r=128 NeoX, "
+             "64 tokens/page, 512 pages/seq, 65536 pages per plane, 2% unmapped",
+}
+
+
+# ------------------------------------------------------------------ utils --
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_sha():
+    import hashlib
+    h = hashlib.sha256()
+    for rel in ("rope_kv_cache_gb300/csrc/ropekv_kernels.cuh", "rope_kv_cache_gb300/csrc/ropekv_api.cu"):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    sha = source_sha()
+    for line in open(path):
+        parts = line.split()
+        if len(parts) >= 4 and not line.startswith("#") and parts[0] == workload and parts[3] == sha:
+            return int(float(parts[2]))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms in a thread."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", gpu_id],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "n_samples": 0}
+        inside = [p for t, p in self.samples if t0 - 0.15 <= t <= t1 + 0.15]
+        note = "during the timed region"
+        if len(inside) < 3:
+            # short timed region: take the samples closest to it
+            near = sorted(self.samples, key=lambda s: abs(s[0] - (t0 + t1) / 2))[:5]
+            inside = [p for _, p in near]
+            note = "nearest samples (timed region shorter than the sampling interval)"
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[1]) for p in inside if num(p[1]) is not None]
+        mx = [num(p[2]) for p in inside if num(p[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in inside for i in range(4)
+                          if p[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "n_samples": len(inside), "window": note}
+
+
+# --------------------------------------------------------- device workload --
+
+class DeviceWorkload:
+    """A workload resident in HBM: a ring of per-step input sets plus the
+    shared cache / pool, and one bound call per ring slot."""
+
+    def __init__(self, name: str, device, l2_bytes: int):
+        import torch
+        import rope_kv_cache_gb300 as rk
+        self.torch = torch
+        self.rk = rk
+        self.name = name
+        self.device = device
+        self.case = workloads.config(name)
+        self.paged = isinstance(self.case, workloads.PagedCase)
+        c = self.case
+        if self.paged:
+            self.tokens = c.valid_rows
+            self.bytes = c.algorithmic_bytes()
+        else:
+            self.tokens = c.tokens
+            self.bytes = c.algorithmic_bytes()
+        self.ring = max(2, min(96, math.ceil(2 * l2_bytes / max(self.bytes, 1))))
+        t = lambda a: self._dev(a)
+        self.sets = []
+        if self.paged:
+            self.pool = self._sentinel(c.pool_shape())
+            k_base, v_base = t(c.k_delta), t(c.v_delta)
+            cs, pos, seq = t(c.cos_sin_rows), t(c.positions), t(c.seq_ids)
+            for k in range(self.ring):
+                pt = t(workloads.step_variant(c, k))
+                self.sets.append(dict(k=k_base.clone() if k else k_base,
+                                      v=v_base.clone() if k else v_base,
+                                      cs=cs.clone() if k else cs, pos=pos, seq=seq, pt=pt))
+            self.bytes = int(np.mean([self._paged_bytes(k) for k in range(self.ring)]))
+        else:
+            self.cos_sin = t(c.cos_sin)
+            self.cache = (t(c.new_cache()) if c.cache_init == "zero"
+                          else self._sentinel((c.B, 2, c.Hkv, c.cap, c.D)))
+            qkv_base = t(c.qkv)
+            for k in range(self.ring):
+                end, pos = workloads.step_variant(c, k)
+                s = dict(qkv=qkv_base.clone() if k else qkv_base)
+                if c.mode != "packed":
+                    s["end"] = t(end)
+                    s["qout"] = self._sentinel((c.B, c.S, c.Hq, c.D))
+                    if c.mode == "tree":
+                        s["pos"] = t(pos)
+                self.sets.append(s)
+        torch.cuda.synchronize(device)
+
+    def _dev(self, a):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            return self.torch.from_numpy(a.view(np.int16)).to(self.device).view(self.torch.float16)
+        return self.torch.from_numpy(a).to(self.device)
+
+    def _sentinel(self, shape):
+        torch = self.torch
+        return torch.full(shape, workloads.SENTINEL, dtype=torch.int16,
+                          device=self.device).view(torch.float16)
+
+    def _paged_bytes(self, k):
+        c = self.case
+        saved = c.page_table
+        c.page_table = workloads.step_variant(c, k)
+        try:
+            return c.algorithmic_bytes()
+        finally:
+            c.page_table = saved
+
+    def footprint(self):
+        return self.ring * self.bytes
+
+    def call(self, k: int, stream):
+        c, s, rk = self.case, self.sets[k % self.ring], self.rk
+        if self.paged:
+            rk.paged_kv_delta_update(s["k"], s["v"], self.pool, s["cs"], s["pos"], s["seq"],
+                                     s["pt"], style=c.style, stream=stream)
+        elif c.mode == "packed":
+            rk.rope_write_kv_packed(self.cos_sin, s["qkv"], self.cache, c.Hq, c.Hkv, c.style,
+                                    stream=stream)
+        elif c.mode == "tree":
+            rk.rope_write_kv_tree(self.cos_sin, s["end"], s["pos"], s["qkv"], self.cache,
+                                  s["qout"], c.Hq, c.Hkv, c.style, stream=stream)
+        else:
+            rk.rope_write_kv_continuous(self.cos_sin, s["end"], s["qkv"], self.cache, s["qout"],
+                                        c.Hq, c.Hkv, c.style, stream=stream)
+
+
+def make_graphs(wl: DeviceWorkload, steps: int, stream, chunk: int = 256):
+    """CUDA graphs holding exactly `steps` launches: full chunks plus a tail."""
+    torch = wl.torch
+    graphs = []
+    k = 0
+    while k < steps:
+        n = min(chunk, steps - k)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for j in range(n):
+                wl.call(k + j, torch.cuda.current_stream())
+        graphs.append(g)
+        k += n
+    return graphs
+
+
+def time_steps(wl: DeviceWorkload, steps: int, warmup: int, stream, barrier=None):
+    """Warm up, then time exactly `steps` launches; returns (seconds, t0, t1)."""
+    torch = wl.torch
+    with torch.cuda.stream(stream):
+        for k in range(warmup):
+            wl.call(k, stream)
+    torch.cuda.synchronize(wl.device)
+    graphs = make_graphs(wl, steps, stream)
+    # CUDAGraph.replay() launches on torch's current stream: make it `stream`,
+    # the stream the events are recorded on.
+    with torch.cuda.stream(stream):
+        # untimed replays: upload the graphs and bring the clocks up
+        spin_end = time.time() + 0.3
+        while True:
+            for g in graphs:
+                g.replay()
+            torch.cuda.synchronize(wl.device)
+            if time.time() >= spin_end:
+                break
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        if barrier:
+            barrier()
+        torch.cuda.synchronize(wl.device)
+        t0 = time.time()
+        start.record(stream)
+        for g in graphs:
+            g.replay()
+        end.record(stream)
+        torch.cuda.synchronize(wl.device)
+        t1 = time.time()
+    if barrier:
+        barrier()
+    sec = start.elapsed_time(end) / 1e3
+    # the host clock around the same region (replay submission + sync) must
+    # agree with the device clock: catches events on a stream the work is not on
+    wall = t1 - t0
+    if wall < 0.9 * sec or (wall > 0.05 and sec < 0.5 * wall):
+        raise RuntimeError(f"event time {sec:.6f}s disagrees with wall time {wall:.6f}s")
+    return sec, t0, t1
+
+
+def e2e_prefill(wl: DeviceWorkload, steps: int, stream):
+    """End to end through the public API: every step copies its QKV and end
+    lengths from pinned host memory, launches, and copies qOut back to pinned
+    host memory (the cache stays resident on the device)."""
+    torch = wl.torch
+    c = wl.case
+    h_qkv = torch.from_numpy(c.qkv.view(np.int16)).pin_memory()
+    h_end = torch.from_numpy(np.ascontiguousarray(c.end_lens)).pin_memory()
+    h_q = torch.empty((c.B, c.S, c.Hq, c.D), dtype=torch.int16).pin_memory()
+    d_qkv = torch.empty(h_qkv.shape, dtype=torch.int16, device=wl.device)
+    d_end = torch.empty(h_end.shape, dtype=torch.int32, device=wl.device)
+    d_q = torch.empty(h_q.shape, dtype=torch.int16, device=wl.device)
+    rk = wl.rk
+
+    def step():
+        d_qkv.copy_(h_qkv, non_blocking=True)
+        d_end.copy_(h_end, non_blocking=True)
+        rk.rope_write_kv_continuous(wl.cos_sin, d_end, d_qkv.view(torch.float16), wl.cache,
+                                    d_q.view(torch.float16), c.Hq, c.Hkv, c.style, stream=stream)
+        h_q.copy_(d_q, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize(wl.device)
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for _ in range(steps):
+            step()
+        end.record(stream)
+    torch.cuda.synchronize(wl.device)
+    sec = start.elapsed_time(end) / 1e3
+    h2d = h_qkv.numel() * 2 + h_end.numel() * 4
+    d2h = h_q.numel() * 2
+    return {"value": c.tokens * steps / sec, "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "steps": steps, "ms_per_step": sec * 1e3 / steps}
+
+
+# ------------------------------------------------------------ CPU oracle --
+
+def oracle_sample(budget_s: float, max_tokens_per_call: int = 2048):
+    """Time the oracle (single thread) on prefill-shaped sub-problems: the
+    first `n` tokens of one sequence at a time, for about budget_s seconds."""
+    import oracle
+    c = workloads.config(HEADLINE)
+    n = min(max_tokens_per_call, c.S)
+    done = 0
+    calls = 0
+    t0 = time.perf_counter()
+    while True:
+        b = calls % c.B
+        qkv = np.ascontiguousarray(c.qkv[b:b + 1, :n])
+        end = np.array([c.end_lens[b] - c.S + n], dtype=np.int32)
+        cache = workloads.sentinel_fill((1, 2, c.Hkv, c.cap, c.D))
+        qout = workloads.sentinel_fill((1, n, c.Hq, c.D))
+        oracle.continuous(c.cos_sin, end, qkv, cache, qout, c.Hq, c.Hkv, c.style)
+        done += n
+        calls += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    sec = time.perf_counter() - t0
+    return done, sec, calls, n
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle as it stands, on the host cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    c = workloads.config(HEADLINE)
+    import oracle
+    oracle.build()
+    # tokens per step sized so warm-up + timed steps take about a minute
+    per_tok_s = 1.0 / 6000.0
+    n = int(max(1, min(c.S, 60.0 / per_tok_s / max(1, args.steps + args.warmup))))
+    b_sub = [np.ascontiguousarray(c.qkv[b:b + 1, :n]) for b in range(c.B)]
+
+    def step(k):
+        b = k % c.B
+        end = np.array([c.end_lens[b] - c.S + n], dtype=np.int32)
+        cache = workloads.sentinel_fill((1, 2, c.Hkv, c.cap, c.D))
+        qout = workloads.sentinel_fill((1, n, c.Hq, c.D))
+        oracle.continuous(c.cos_sin, end, b_sub[b], cache, qout, c.Hq, c.Hkv, c.style)
+
+    for k in range(args.warmup):
+        step(k)
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        step(k)
+    sec = time.perf_counter() - t0
+    value = n * args.steps / sec
+    sample = f"oracle.continuous, single thread, {n} tokens of one prefill sequence per step"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": sec * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1) FP16 QKV)",
+        "config": {"workload": DESCR[HEADLINE], "tokens_per_step": n},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------- main --
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--extra-steps", type=int, default=4000,
+                    help="timed launches per extra workload (decode, tree, paged, packed_tiny)")
+    ap.add_argument("--no-extra", action="store_true", help="headline workload only")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="CPU time budget of the oracle baseline sample")
+    ap.add_argument("--e2e-steps", type=int, default=100)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != args.gpus:
+        if world > 1 or args.gpus > 1:
+            raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE={world}: launch with torchrun")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    barrier = None
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        barrier = lambda: dist.barrier()
+
+    from rope_kv_cache_gb300 import build as rkbuild
+    rkbuild.build_library()
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 0) or 126 * 2 ** 20)
+    peak, peak_src = measured_peak()
+    uuid = str(getattr(props, "uuid", "") or "")
+    gpu_id = ("GPU-" + uuid) if uuid and not uuid.startswith("GPU-") else (uuid or str(local))
+    sampler = ClockSampler(gpu_id) if rank == 0 else None
+    stream = torch.cuda.Stream(dev)
+
+    wl = DeviceWorkload(HEADLINE, dev, l2)
+    sec, t0, t1 = time_steps(wl, args.steps, args.warmup, stream, barrier)
+    if world > 1:
+        t = torch.tensor([sec], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        sec = float(t.item())
+    launch_s = sec / args.steps
+    achieved = wl.bytes / launch_s / 1e9
+    clocks = sampler.summary(t0, t1) if sampler else None
+    e2e = e2e_prefill(wl, args.e2e_steps, stream)
+
+    extra = {}
+    if not args.no_extra:
+        wl_cache = wl.cache
+        del wl, wl_cache
+        torch.cuda.empty_cache()
+        for name in EXTRA:
+            w = DeviceWorkload(name, dev, l2)
+            s, _, _ = time_steps(w, args.extra_steps, args.warmup, stream, barrier)
+            per = s / args.extra_steps
+            gbs = w.bytes / per / 1e9
+            extra[name] = {"workload": DESCR[name], "tokens_per_step": w.tokens,
+                           "bytes_per_step": w.bytes, "ring": w.ring,
+                           "us_per_launch": per * 1e6, "tokens_per_s": w.tokens / per,
+                           "effective_gbs": gbs, "frac_of_measured_peak": gbs / peak,
+                           "frac_of_nominal_8tbs": gbs / NOMINAL_HBM_GBS,
+                           "launches_timed": args.extra_steps,
+                           "dram_bytes_per_launch_ncu": ncu_traffic(name)}
+            del w
+            torch.cuda.empty_cache()
+    else:
+        del wl
+    if sampler:
+        sampler.stop()
+    if world > 1:
+        dist.destroy_process_group()
+    if rank != 0:
+        return 0
+
+    case = workloads.config(HEADLINE)
+    tokens = case.tokens
+    bytes_step = case.algorithmic_bytes()
+    cpu_tokens, cpu_sec, cpu_calls, cpu_n = oracle_sample(args.cpu_seconds)
+    line = {
+        "metric": METRIC,
+        "value": world * tokens * args.steps / sec,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": sec * 1e3 / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "storage": "f16 in/out, f32 cos/sin, f32 math",
+        "data": "synthetic: seeded N(0,1) FP16 activations, FP32 RoPE table (no dataset, no weights)",
+        "config": {"workload": DESCR[HEADLINE], "tokens_per_step": tokens,
+                   "bytes_per_step": bytes_step},
+        "effective_gbs": achieved,
+        "pct_of_peak": {"measured_copy": 100 * achieved / peak,
+                        "nominal_8tbs": 100 * achieved / NOMINAL_HBM_GBS},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": ncu_traffic(HEADLINE),
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_src == "measured" else "fallback 6.8 TB/s",
+                     "kernel": "rope_kv_token_kernel<128, NeoX, continuous>"},
+        "cpu_baseline": {"value": cpu_tokens / cpu_sec, "unit": "tokens/s", "cores": 1,
+                         "kind": "oracle",
+                         "sample": f"{cpu_calls} calls of oracle.continuous on {cpu_n} tokens of "
+                                   f"one prefill sequence ({cpu_tokens} tokens, {cpu_sec:.1f} s)"},
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "workloads": extra,
+    }
+    line["config"]["l2"] = (f"inputs larger than L2: ring of {_ring_of(tokens, bytes_step, l2)} "
+                            f"input sets, {_ring_of(tokens, bytes_step, l2) * bytes_step / 1e6:.0f} MB "
+                            f"> 2 x L2 ({l2 / 1e6:.0f} MB)")
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def _ring_of(tokens, bytes_step, l2):
+    return max(2, min(96, math.ceil(2 * l2 / max(bytes_step, 1))))
+
+
+if __name__ == "__main__":
+    sys.exit(main())

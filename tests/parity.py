@@ -35,6 +35,12 @@ def to_dev(a: np.ndarray):
     return torch.from_numpy(a).to(dev())
 
 
+def dev_sentinel(shape):
+    """A device FP16 buffer filled with the sentinel bits, made on the device."""
+    return torch.full(tuple(shape), workloads.SENTINEL, dtype=torch.int16,
+                      device=dev()).view(torch.float16)
+
+
 def to_host_bits(t) -> np.ndarray:
     return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
 

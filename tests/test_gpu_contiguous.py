@@ -10,8 +10,8 @@ import numpy as np
 import pytest
 
 import workloads
-from parity import (cache_rotated, check_contiguous, compare, qout_rotated, to_dev,
-                    to_host_bits)
+from parity import (cache_rotated, check_contiguous, compare, dev_sentinel, qout_rotated,
+                    to_dev, to_host_bits)
 
 pytestmark = pytest.mark.gpu
 
@@ -155,8 +155,8 @@ def test_config_written_slots_and_untouched(name):
     cs = to_dev(case.cos_sin)
     qkv = to_dev(case.qkv)
     end = to_dev(case.end_lens)
-    cache = to_dev(case.new_cache())
-    qout = to_dev(case.new_qout())
+    cache = dev_sentinel((case.B, 2, case.Hkv, case.cap, case.D))
+    qout = dev_sentinel((case.B, case.S, case.Hq, case.D))
     if case.mode == "tree":
         rk.rope_write_kv_tree(cs, end, to_dev(case.pos_ids), qkv, cache, qout, case.Hq, case.Hkv,
                               case.style)

@@ -9,7 +9,7 @@ import numpy as np
 import pytest
 
 import workloads
-from parity import compare, pool_rotated, to_dev, to_host_bits
+from parity import compare, dev_sentinel, pool_rotated, to_dev, to_host_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -27,7 +27,7 @@ def _built():
 
 def _run_gpu(pc, batch_size=None, stream=None):
     import rope_kv_cache_gb300 as rk
-    pool = to_dev(pc.new_pool())
+    pool = dev_sentinel(pc.pool_shape())
     rk.paged_kv_delta_update(to_dev(pc.k_delta), to_dev(pc.v_delta), pool, to_dev(pc.cos_sin_rows),
                              to_dev(pc.positions), to_dev(pc.seq_ids), to_dev(pc.page_table),
                              batch_size=batch_size, style=pc.style, stream=stream)
