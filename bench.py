@@ -54,6 +54,8 @@ DESCR = {
             "depth 0..6, base in [128,4000], capacity 4096",
     "paged": "paged delta update: 16384 rows (15565 valid) over B=128, Hkv=8 D=r=128 NeoX, "
              "64 tokens/page, 512 pages/seq, 65536 pages per plane, 2% unmapped",
+    "decode_c1024": "decode as above with cache capacity 1024 (profiler-sized twin)",
+    "paged_p8192": "paged as above with 64 pages/seq and 8192 pages per plane (profiler-sized twin)",
 }
 
 
@@ -298,43 +300,83 @@ def time_steps(wl: DeviceWorkload, steps: int, warmup: int, stream, barrier=None
     return sec, t0, t1
 
 
-def e2e_prefill(wl: DeviceWorkload, steps: int, stream):
-    """End to end through the public API: every step copies its QKV and end
-    lengths from pinned host memory, launches, and copies qOut back to pinned
-    host memory (the cache stays resident on the device)."""
+def e2e_contiguous(wl: DeviceWorkload, steps: int):
+    """End to end through the public API with host buffers.
+
+    Every step copies its inputs (QKV, end lengths, tree positions) from pinned
+    host memory to the device, launches the entry point, and copies its output
+    (qOut; the rotated QKV for the packed call) back to pinned host memory; the
+    cache stays resident on the device. Steps are software-pipelined over two
+    device buffer sets and three streams, so the host-to-device copy of step k+1
+    and the device-to-host copy of step k-1 overlap the kernel of step k.
+    """
     torch = wl.torch
     c = wl.case
-    h_qkv = torch.from_numpy(c.qkv.view(np.int16)).pin_memory()
-    h_end = torch.from_numpy(np.ascontiguousarray(c.end_lens)).pin_memory()
-    h_q = torch.empty((c.B, c.S, c.Hq, c.D), dtype=torch.int16).pin_memory()
-    d_qkv = torch.empty(h_qkv.shape, dtype=torch.int16, device=wl.device)
-    d_end = torch.empty(h_end.shape, dtype=torch.int32, device=wl.device)
-    d_q = torch.empty(h_q.shape, dtype=torch.int16, device=wl.device)
+    dev = wl.device
+    h_in = {"qkv": torch.from_numpy(c.qkv.view(np.int16)).pin_memory()}
+    if c.mode != "packed":
+        h_in["end"] = torch.from_numpy(np.ascontiguousarray(c.end_lens)).pin_memory()
+    if c.mode == "tree":
+        h_in["pos"] = torch.from_numpy(np.ascontiguousarray(c.pos_ids)).pin_memory()
+    out_shape = tuple(c.qkv.shape) if c.mode == "packed" else (c.B, c.S, c.Hq, c.D)
+    h_out = torch.empty(out_shape, dtype=torch.int16).pin_memory()
+    d_in = [{k: torch.empty(v.shape, dtype=v.dtype, device=dev) for k, v in h_in.items()}
+            for _ in range(2)]
+    # the packed call rotates its input in place: its output buffer is the input
+    d_out = [d["qkv"] if c.mode == "packed" else
+             torch.empty(out_shape, dtype=torch.int16, device=dev) for d in d_in]
+    s_h2d, s_cmp, s_d2h = (torch.cuda.Stream(dev) for _ in range(3))
+    ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("h2d", "cmp", "d2h")}
     rk = wl.rk
 
-    def step():
-        d_qkv.copy_(h_qkv, non_blocking=True)
-        d_end.copy_(h_end, non_blocking=True)
-        rk.rope_write_kv_continuous(wl.cos_sin, d_end, d_qkv.view(torch.float16), wl.cache,
-                                    d_q.view(torch.float16), c.Hq, c.Hkv, c.style, stream=stream)
-        h_q.copy_(d_q, non_blocking=True)
+    def step(k):
+        j = k % 2
+        with torch.cuda.stream(s_h2d):
+            if k >= 2:
+                s_h2d.wait_event(ev["cmp"][j])      # kernel k-2 has read set j
+                s_h2d.wait_event(ev["d2h"][j])      # and its output has been copied out
+            for name, h in h_in.items():
+                d_in[j][name].copy_(h, non_blocking=True)
+            ev["h2d"][j].record(s_h2d)
+        with torch.cuda.stream(s_cmp):
+            s_cmp.wait_event(ev["h2d"][j])
+            if k >= 2:
+                s_cmp.wait_event(ev["d2h"][j])      # output of step k-2 copied out
+            x = d_in[j]
+            if c.mode == "packed":
+                rk.rope_write_kv_packed(wl.cos_sin, x["qkv"].view(torch.float16), wl.cache,
+                                        c.Hq, c.Hkv, c.style, stream=s_cmp)
+            elif c.mode == "tree":
+                rk.rope_write_kv_tree(wl.cos_sin, x["end"], x["pos"], x["qkv"].view(torch.float16),
+                                      wl.cache, d_out[j].view(torch.float16), c.Hq, c.Hkv,
+                                      c.style, stream=s_cmp)
+            else:
+                rk.rope_write_kv_continuous(wl.cos_sin, x["end"], x["qkv"].view(torch.float16),
+                                            wl.cache, d_out[j].view(torch.float16), c.Hq, c.Hkv,
+                                            c.style, stream=s_cmp)
+            ev["cmp"][j].record(s_cmp)
+        with torch.cuda.stream(s_d2h):
+            s_d2h.wait_event(ev["cmp"][j])
+            h_out.copy_(d_out[j], non_blocking=True)
+            ev["d2h"][j].record(s_d2h)
 
-    with torch.cuda.stream(stream):
-        for _ in range(3):
-            step()
-        torch.cuda.synchronize(wl.device)
-        start = torch.cuda.Event(enable_timing=True)
-        end = torch.cuda.Event(enable_timing=True)
-        start.record(stream)
-        for _ in range(steps):
-            step()
-        end.record(stream)
-    torch.cuda.synchronize(wl.device)
+    for k in range(3):
+        step(k)
+    torch.cuda.synchronize(dev)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(s_h2d)
+    for k in range(steps):
+        step(k)
+    s_d2h.wait_event(ev["d2h"][(steps - 1) % 2])
+    end.record(s_d2h)
+    torch.cuda.synchronize(dev)
     sec = start.elapsed_time(end) / 1e3
-    h2d = h_qkv.numel() * 2 + h_end.numel() * 4
-    d2h = h_q.numel() * 2
+    h2d = sum(v.numel() * v.element_size() for v in h_in.values())
+    d2h = h_out.numel() * h_out.element_size()
     return {"value": c.tokens * steps / sec, "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h), "steps": steps, "ms_per_step": sec * 1e3 / steps}
+            "d2h_bytes_per_step": int(d2h), "steps": steps, "ms_per_step": sec * 1e3 / steps,
+            "pipelined": "H2D of step k+1 and D2H of step k-1 overlap the kernel of step k"}
 
 
 # ------------------------------------------------------------ CPU oracle --
@@ -414,6 +456,9 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=HEADLINE,
+                    choices=list(workloads.CONFIG_NAMES) + list(workloads.PROFILE_NAMES),
+                    help="workload of the headline line (default: the prefill)")
     ap.add_argument("--extra-steps", type=int, default=4000,
                     help="timed launches per extra workload (decode, tree, paged, packed_tiny)")
     ap.add_argument("--no-extra", action="store_true", help="headline workload only")
@@ -430,9 +475,8 @@ def main(argv=None):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world != args.gpus:
-        if world > 1 or args.gpus > 1:
-            raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE={world}: launch with torchrun")
+    if world != args.gpus and (world > 1 or args.gpus > 1):
+        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE={world}: launch with torchrun")
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     barrier = None
@@ -452,7 +496,8 @@ def main(argv=None):
     sampler = ClockSampler(gpu_id) if rank == 0 else None
     stream = torch.cuda.Stream(dev)
 
-    wl = DeviceWorkload(HEADLINE, dev, l2)
+    name = args.workload
+    wl = DeviceWorkload(name, dev, l2)
     sec, t0, t1 = time_steps(wl, args.steps, args.warmup, stream, barrier)
     if world > 1:
         t = torch.tensor([sec], device=dev, dtype=torch.float64)
@@ -461,29 +506,30 @@ def main(argv=None):
     launch_s = sec / args.steps
     achieved = wl.bytes / launch_s / 1e9
     clocks = sampler.summary(t0, t1) if sampler else None
-    e2e = e2e_prefill(wl, args.e2e_steps, stream)
+    e2e = e2e_contiguous(wl, args.e2e_steps) if not wl.paged else None
+    tokens, bytes_step, ring = wl.tokens, wl.bytes, wl.ring
+    kernel = _kernel_name(wl)
+    del wl
+    torch.cuda.empty_cache()
 
     extra = {}
     if not args.no_extra:
-        wl_cache = wl.cache
-        del wl, wl_cache
-        torch.cuda.empty_cache()
-        for name in EXTRA:
-            w = DeviceWorkload(name, dev, l2)
-            s, _, _ = time_steps(w, args.extra_steps, args.warmup, stream, barrier)
-            per = s / args.extra_steps
+        for xname in EXTRA:
+            if xname == name:
+                continue
+            w = DeviceWorkload(xname, dev, l2)
+            s_, _, _ = time_steps(w, args.extra_steps, args.warmup, stream, barrier)
+            per = s_ / args.extra_steps
             gbs = w.bytes / per / 1e9
-            extra[name] = {"workload": DESCR[name], "tokens_per_step": w.tokens,
-                           "bytes_per_step": w.bytes, "ring": w.ring,
-                           "us_per_launch": per * 1e6, "tokens_per_s": w.tokens / per,
-                           "effective_gbs": gbs, "frac_of_measured_peak": gbs / peak,
-                           "frac_of_nominal_8tbs": gbs / NOMINAL_HBM_GBS,
-                           "launches_timed": args.extra_steps,
-                           "dram_bytes_per_launch_ncu": ncu_traffic(name)}
+            extra[xname] = {"workload": DESCR[xname], "tokens_per_step": w.tokens,
+                            "bytes_per_step": w.bytes, "ring": w.ring,
+                            "us_per_launch": per * 1e6, "tokens_per_s": w.tokens / per,
+                            "effective_gbs": gbs, "frac_of_measured_peak": gbs / peak,
+                            "frac_of_nominal_8tbs": gbs / NOMINAL_HBM_GBS,
+                            "launches_timed": args.extra_steps, "kernel": _kernel_name(w),
+                            "dram_bytes_per_launch_ncu": ncu_traffic(xname)}
             del w
             torch.cuda.empty_cache()
-    else:
-        del wl
     if sampler:
         sampler.stop()
     if world > 1:
@@ -491,9 +537,6 @@ def main(argv=None):
     if rank != 0:
         return 0
 
-    case = workloads.config(HEADLINE)
-    tokens = case.tokens
-    bytes_step = case.algorithmic_bytes()
     cpu_tokens, cpu_sec, cpu_calls, cpu_n = oracle_sample(args.cpu_seconds)
     line = {
         "metric": METRIC,
@@ -509,16 +552,18 @@ def main(argv=None):
         "dtype": "f32",
         "storage": "f16 in/out, f32 cos/sin, f32 math",
         "data": "synthetic: seeded N(0,1) FP16 activations, FP32 RoPE table (no dataset, no weights)",
-        "config": {"workload": DESCR[HEADLINE], "tokens_per_step": tokens,
-                   "bytes_per_step": bytes_step},
+        "config": {"workload": DESCR.get(name, name), "tokens_per_step": tokens,
+                   "bytes_per_step": bytes_step,
+                   "l2": f"inputs larger than L2: ring of {ring} input sets, "
+                         f"{ring * bytes_step / 1e6:.0f} MB > 2 x L2 ({l2 / 1e6:.0f} MB)"},
         "effective_gbs": achieved,
         "pct_of_peak": {"measured_copy": 100 * achieved / peak,
                         "nominal_8tbs": 100 * achieved / NOMINAL_HBM_GBS},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": ncu_traffic(HEADLINE),
-                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
+                     "frac": achieved / peak, "traffic": ncu_traffic(name),
+                     "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs, burst copy)"
                      if peak_src == "measured" else "fallback 6.8 TB/s",
-                     "kernel": "rope_kv_token_kernel<128, NeoX, continuous>"},
+                     "kernel": kernel},
         "cpu_baseline": {"value": cpu_tokens / cpu_sec, "unit": "tokens/s", "cores": 1,
                          "kind": "oracle",
                          "sample": f"{cpu_calls} calls of oracle.continuous on {cpu_n} tokens of "
@@ -528,15 +573,16 @@ def main(argv=None):
         "clocks": clocks,
         "workloads": extra,
     }
-    line["config"]["l2"] = (f"inputs larger than L2: ring of {_ring_of(tokens, bytes_step, l2)} "
-                            f"input sets, {_ring_of(tokens, bytes_step, l2) * bytes_step / 1e6:.0f} MB "
-                            f"> 2 x L2 ({l2 / 1e6:.0f} MB)")
     print(json.dumps(line), flush=True)
     return 0
 
 
-def _ring_of(tokens, bytes_step, l2):
-    return max(2, min(96, math.ceil(2 * l2 / max(bytes_step, 1))))
+def _kernel_name(wl) -> str:
+    c = wl.case
+    if wl.paged:
+        return f"paged_delta_kernel<D={c.D}, {'NeoX' if c.style == 0 else 'GPT-J'}>"
+    return (f"rope_kv_token_kernel<D={c.D}, {'NeoX' if c.style == 0 else 'GPT-J'}, "
+            f"{c.mode}>")
 
 
 if __name__ == "__main__":

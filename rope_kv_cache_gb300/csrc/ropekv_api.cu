@@ -14,8 +14,6 @@ namespace {
 using ropekv::PagedArgs;
 using ropekv::TokenArgs;
 
-constexpr int kMaxThreads = 256;
-
 bool aligned16(const void* p)
 {
     return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
@@ -31,9 +29,15 @@ int check_head_dims(int32_t D, int32_t r)
 }
 
 // Launch shape for `units` tokens (or rows) of `items` items each.
-// IPT = items per thread; CTAs per unit split a unit's items evenly over
-// blocks of at most 256 threads, rounded to whole warps (a warp size is a
-// multiple of every D/16, which keeps each thread on one item index).
+// Measured on GB300 over the prefill, decode, tree and paged workloads:
+//   * large launches (>= 1024 units): 64-thread CTAs with two items per thread
+//     (128 items = 16 heads of 128 dims per CTA) keep the CTA launch rate and
+//     the bytes in flight per SM balanced; bigger CTAs lose 2-5 % on the
+//     shorter tree/paged launches, smaller ones run into the CTA launch rate;
+//   * small launches (decode): one item per thread, up to 192 items per CTA,
+//     which spreads the few tokens over more SMs.
+// Blocks are whole warps; a warp's size is a multiple of every D/16, which
+// keeps each thread on one item index.
 struct Shape {
     int threads;
     int ipt;
@@ -43,18 +47,30 @@ struct Shape {
 Shape pick_shape(int items, long long units)
 {
     Shape sh;
-    sh.ipt = (units >= 1024) ? 2 : 1;
-    sh.ctasPerUnit = (items + kMaxThreads * sh.ipt - 1) / (kMaxThreads * sh.ipt);
-    int per = (items + sh.ctasPerUnit * sh.ipt - 1) / (sh.ctasPerUnit * sh.ipt);
+    int perCta;
+    if (units >= 1024) {
+        sh.ipt = 2;
+        perCta = 128;
+    } else {
+        sh.ipt = 1;
+        perCta = 192;
+    }
+    sh.ctasPerUnit = (items + perCta - 1) / perCta;
+    const int per = (items + sh.ctasPerUnit * sh.ipt - 1) / (sh.ctasPerUnit * sh.ipt);
     sh.threads = ((per + 31) / 32) * 32;
     return sh;
 }
+
+// Kernel policy of every launch: streaming L2 hints on activations and cache
+// rows (see ropekv_kernels.cuh). Programmatic dependent launch is left off: on
+// launches of tens of thousands of CTAs it lowered the CTA launch rate.
+constexpr int kPolicy = ropekv::kStreamHint;
 
 template <int D, int STYLE, int MODE, int IPT>
 void launch_token(const TokenArgs& a, long long tokens, const Shape& sh, cudaStream_t st)
 {
     const unsigned grid = (unsigned)(tokens * sh.ctasPerUnit);
-    ropekv::rope_kv_token_kernel<D, STYLE, MODE, IPT><<<grid, sh.threads, 0, st>>>(a);
+    ropekv::rope_kv_token_kernel<D, STYLE, MODE, IPT, kPolicy><<<grid, sh.threads, 0, st>>>(a);
 }
 
 template <int D, int STYLE, int MODE>
@@ -92,9 +108,9 @@ void launch_paged(const PagedArgs& a, long long rows, const Shape& sh, cudaStrea
 {
     const unsigned grid = (unsigned)(rows * sh.ctasPerUnit);
     if (sh.ipt == 2)
-        ropekv::paged_delta_kernel<D, STYLE, 2><<<grid, sh.threads, 0, st>>>(a);
+        ropekv::paged_delta_kernel<D, STYLE, 2, kPolicy><<<grid, sh.threads, 0, st>>>(a);
     else
-        ropekv::paged_delta_kernel<D, STYLE, 1><<<grid, sh.threads, 0, st>>>(a);
+        ropekv::paged_delta_kernel<D, STYLE, 1, kPolicy><<<grid, sh.threads, 0, st>>>(a);
 }
 
 template <int D>

@@ -67,23 +67,94 @@ struct PagedArgs {
 
 // --------------------------------------------------------------- helpers --
 
-__device__ __forceinline__ uint4 load_ro(const uint16_t* p)
+// Compile-time memory/launch policy of a kernel instantiation (bit set).
+//   kPdl:        the grid may be launched as a programmatic dependent of the
+//                previous kernel in the stream. Every thread first lets the
+//                next grid begin launching, then waits until the previous
+//                grid has completed and its writes are visible, before it
+//                reads or writes anything: safe whatever that grid did.
+//   kStreamHint: activations and cache rows are touched once per call: load
+//                them bypassing L1 and mark loads and stores evict-first in L2.
+//   kTableKeep:  cos/sin rows are reused by every call: mark them evict-last
+//                in L2 so the streaming traffic does not push them out.
+enum Policy : int { kPdl = 1, kStreamHint = 2, kTableKeep = 4 };
+
+struct L2Policies {
+    uint64_t stream;
+    uint64_t keep;
+};
+
+template <int POL>
+__device__ __forceinline__ L2Policies make_policies()
 {
+    L2Policies p{0, 0};
+    if (POL & kStreamHint)
+        asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p.stream));
+    if (POL & kTableKeep)
+        asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p.keep));
+    return p;
+}
+
+template <int POL>
+__device__ __forceinline__ void grid_dependency_sync()
+{
+    if (POL & kPdl) {
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+    }
+}
+
+// 16-byte load of data that no thread of this grid writes.
+template <int POL>
+__device__ __forceinline__ uint4 load_ro(const uint16_t* p, const L2Policies& pol)
+{
+    if (POL & kStreamHint) {
+        uint4 v;
+        asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+                     : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                     : "l"(p), "l"(pol.stream));
+        return v;
+    }
     return __ldg(reinterpret_cast<const uint4*>(p));
 }
 
-__device__ __forceinline__ uint4 load_rw(const uint16_t* p)
+// 16-byte load of data this grid later overwrites (the packed in-place call).
+template <int POL>
+__device__ __forceinline__ uint4 load_rw(const uint16_t* p, const L2Policies& pol)
 {
+    if (POL & kStreamHint) {
+        uint4 v;
+        asm volatile("ld.global.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+                     : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                     : "l"(p), "l"(pol.stream)
+                     : "memory");
+        return v;
+    }
     return *reinterpret_cast<const uint4*>(p);
 }
 
-__device__ __forceinline__ void store_v(uint16_t* p, const uint4& v)
+template <int POL>
+__device__ __forceinline__ void store_v(uint16_t* p, const uint4& v, const L2Policies& pol)
 {
+    if (POL & kStreamHint) {
+        asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1,%2,%3,%4}, %5;"
+                     :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "l"(pol.stream)
+                     : "memory");
+        return;
+    }
     *reinterpret_cast<uint4*>(p) = v;
 }
 
-__device__ __forceinline__ float4 load_f4(const float* p)
+template <int POL>
+__device__ __forceinline__ float4 load_f4(const float* p, const L2Policies& pol)
 {
+    if (POL & kTableKeep) {
+        float4 f;
+        asm volatile("ld.global.nc.L2::cache_hint.v4.f32 {%0,%1,%2,%3}, [%4], %5;"
+                     : "=f"(f.x), "=f"(f.y), "=f"(f.z), "=f"(f.w)
+                     : "l"(p), "l"(pol.keep));
+        return f;
+    }
     return __ldg(reinterpret_cast<const float4*>(p));
 }
 
@@ -110,22 +181,22 @@ __device__ __forceinline__ void item_vectors(int i, int r, int& va, int& vb)
 // cos/sin of the frequencies item i uses, from one table row of r floats.
 // NeoX: frequencies 8i..8i+7 (shared by both vectors).
 // GPT-J: frequencies 4i..4i+3 (first vector) and r/4 + 4i .. +3 (second).
-template <int STYLE>
+template <int STYLE, int POL>
 __device__ __forceinline__ void load_cos_sin(const float* row, int i, int r, float c[8],
-                                             float s[8])
+                                             float s[8], const L2Policies& pol)
 {
     const int h = r >> 1;
     float4 a, b, e, f;
     if (STYLE == kNeox) {
-        a = load_f4(row + 8 * i);
-        b = load_f4(row + 8 * i + 4);
-        e = load_f4(row + h + 8 * i);
-        f = load_f4(row + h + 8 * i + 4);
+        a = load_f4<POL>(row + 8 * i, pol);
+        b = load_f4<POL>(row + 8 * i + 4, pol);
+        e = load_f4<POL>(row + h + 8 * i, pol);
+        f = load_f4<POL>(row + h + 8 * i + 4, pol);
     } else {
-        a = load_f4(row + 4 * i);
-        b = load_f4(row + 4 * i + (r >> 2));
-        e = load_f4(row + h + 4 * i);
-        f = load_f4(row + h + 4 * i + (r >> 2));
+        a = load_f4<POL>(row + 4 * i, pol);
+        b = load_f4<POL>(row + 4 * i + (r >> 2), pol);
+        e = load_f4<POL>(row + h + 4 * i, pol);
+        f = load_f4<POL>(row + h + 4 * i + (r >> 2), pol);
     }
     c[0] = a.x; c[1] = a.y; c[2] = a.z; c[3] = a.w;
     c[4] = b.x; c[5] = b.y; c[6] = b.z; c[7] = b.w;
@@ -186,10 +257,12 @@ __device__ __forceinline__ void rotate_item(uint4& va, uint4& vb, const float c[
 // Grid: tokens * ctasPerToken CTAs; CTA (token, part) covers items
 // [part * blockDim * IPT, (part + 1) * blockDim * IPT) of the token, each thread
 // items tid + k * blockDim for k < IPT. blockDim is a multiple of D/16.
-template <int D, int STYLE, int MODE, int IPT>
+template <int D, int STYLE, int MODE, int IPT, int POL>
 __global__ void __launch_bounds__(256) rope_kv_token_kernel(const TokenArgs a)
 {
     constexpr int kItemsPerHead = D / 16;
+    grid_dependency_sync<POL>();
+    const L2Policies pol = make_policies<POL>();
     const int tok = blockIdx.x / a.ctasPerToken;
     const int part = blockIdx.x - tok * a.ctasPerToken;
     const int b = tok / a.S;
@@ -211,11 +284,11 @@ __global__ void __launch_bounds__(256) rope_kv_token_kernel(const TokenArgs a)
             const int head = item / kItemsPerHead;
             const uint16_t* p = tokIn + (size_t)head * D;
             if (MODE == kPacked) {
-                xa[k] = load_rw(p + 8 * va);
-                xb[k] = load_rw(p + 8 * vb);
+                xa[k] = load_rw<POL>(p + 8 * va, pol);
+                xb[k] = load_rw<POL>(p + 8 * vb, pol);
             } else {
-                xa[k] = load_ro(p + 8 * va);
-                xb[k] = load_ro(p + 8 * vb);
+                xa[k] = load_ro<POL>(p + 8 * va, pol);
+                xb[k] = load_ro<POL>(p + 8 * vb, pol);
             }
         }
     }
@@ -238,7 +311,7 @@ __global__ void __launch_bounds__(256) rope_kv_token_kernel(const TokenArgs a)
     if (rotItem) {
         const int bc = (a.csBatch == 1) ? 0 : b;
         const float* row = a.cosSin + ((size_t)bc * a.csSeq + pos) * a.r;
-        load_cos_sin<STYLE>(row, i, a.r, c, sn);
+        load_cos_sin<STYLE, POL>(row, i, a.r, c, sn, pol);
     }
 
     // 4. rotate and store
@@ -259,8 +332,8 @@ __global__ void __launch_bounds__(256) rope_kv_token_kernel(const TokenArgs a)
                 const int hk = head - a.Hq;
                 if (MODE == kPacked) {
                     uint16_t* q = a.qkvOut + (size_t)tok * H * D + (size_t)head * D;
-                    store_v(q + 8 * va, xa[k]);
-                    store_v(q + 8 * vb, xb[k]);
+                    store_v<POL>(q + 8 * va, xa[k], pol);
+                    store_v<POL>(q + 8 * vb, xb[k], pol);
                 }
                 dst = a.cache + ((((size_t)b * 2 + 0) * a.Hkv + hk) * a.cap + slot) * D;
             }
@@ -268,8 +341,8 @@ __global__ void __launch_bounds__(256) rope_kv_token_kernel(const TokenArgs a)
             const int hv = head - a.Hq - a.Hkv;
             dst = a.cache + ((((size_t)b * 2 + 1) * a.Hkv + hv) * a.cap + slot) * D;
         }
-        store_v(dst + 8 * va, xa[k]);
-        store_v(dst + 8 * vb, xb[k]);
+        store_v<POL>(dst + 8 * va, xa[k], pol);
+        store_v<POL>(dst + 8 * vb, xb[k], pol);
     }
 }
 
@@ -277,10 +350,12 @@ __global__ void __launch_bounds__(256) rope_kv_token_kernel(const TokenArgs a)
 //
 // Grid: rows * ctasPerRow CTAs; items [0, Hkv*D/16) are K heads, the rest V
 // heads, split across the CTAs of a row like the token kernel.
-template <int D, int STYLE, int IPT>
+template <int D, int STYLE, int IPT, int POL>
 __global__ void __launch_bounds__(256) paged_delta_kernel(const PagedArgs a)
 {
     constexpr int kItemsPerHead = D / 16;
+    grid_dependency_sync<POL>();
+    const L2Policies pol = make_policies<POL>();
     const int t = blockIdx.x / a.ctasPerRow;
     const int part = blockIdx.x - t * a.ctasPerRow;
     const int i = threadIdx.x % kItemsPerHead;
@@ -309,8 +384,8 @@ __global__ void __launch_bounds__(256) paged_delta_kernel(const PagedArgs a)
             const bool isK = item < kItems;
             const int head = (isK ? item : item - kItems) / kItemsPerHead;
             const uint16_t* p = (isK ? a.kDelta : a.vDelta) + rowOff + (size_t)head * D;
-            xa[k] = load_ro(p + 8 * va);
-            xb[k] = load_ro(p + 8 * vb);
+            xa[k] = load_ro<POL>(p + 8 * va, pol);
+            xb[k] = load_ro<POL>(p + 8 * vb, pol);
         }
     }
 
@@ -323,7 +398,7 @@ __global__ void __launch_bounds__(256) paged_delta_kernel(const PagedArgs a)
     float c[8], sn[8];
     const bool rotItem = i < (a.r >> 4);
     if (rotItem && kOk)
-        load_cos_sin<STYLE>(a.cosSin + (size_t)t * a.r, i, a.r, c, sn);
+        load_cos_sin<STYLE, POL>(a.cosSin + (size_t)t * a.r, i, a.r, c, sn, pol);
 
     const size_t rowElems = (size_t)a.Hkv * D;
 #pragma unroll
@@ -339,8 +414,8 @@ __global__ void __launch_bounds__(256) paged_delta_kernel(const PagedArgs a)
             rotate_item<STYLE>(xa[k], xb[k], c, sn);
         const int id = isK ? idK : idV;  // flat page index of the [2, numPages] pool
         uint16_t* dst = a.pool + ((size_t)id * a.tpp + inPage) * rowElems + (size_t)head * D;
-        store_v(dst + 8 * va, xa[k]);
-        store_v(dst + 8 * vb, xb[k]);
+        store_v<POL>(dst + 8 * va, xa[k], pol);
+        store_v<POL>(dst + 8 * vb, xb[k], pol);
     }
 }
 

@@ -304,6 +304,11 @@ def make_paged(N, B, Hkv, D, r, tokens_per_page, max_pages_per_seq, num_pages, s
 
 CONFIG_NAMES = ("packed_tiny", "prefill", "decode", "tree", "paged")
 
+# Smaller-footprint twins of two workloads for profiler captures: the same
+# tokens / rows per launch, a smaller cache (decode: capacity 1024) or pool
+# (paged: 64 logical pages per sequence, 8192 pages per plane, positions < 4096).
+PROFILE_NAMES = ("decode_c1024", "paged_p8192")
+
 
 def config(name: str):
     """The five benchmark workloads, each drawn with its own seed (0..4)."""
@@ -330,6 +335,16 @@ def config(name: str):
         # [128, 4000], capacity 4096.
         return make_tree(64, 64, 32, 8, 128, 64, 4096, GPTJ, 1e4, seed=3,
                          base_range=(128, 4000), cs_seq=4096, name=name)
+    if name == "decode_c1024":
+        rng = rng_for(2)
+        qkv = fp16_normal(rng, (256, 1, 48, 128))
+        end_lens = rng.integers(1, 1024 + 1, size=256).astype(np.int32)
+        cos_sin = cos_sin_table(5e5, 1024, 128)
+        return ContiguousCase("continuous", 256, 1, 32, 8, 128, 128, 1024, NEOX, 5e5, cos_sin,
+                              qkv, end_lens=end_lens, name=name)
+    if name == "paged_p8192":
+        return make_paged(16384, 128, 8, 128, 128, 64, 64, 8192, NEOX, 5e5, seed=4,
+                          valid_rows=15565, name=name)
     if name == "paged":
         # 16384 delta rows over 128 sequences (15565 valid), Hkv=8, D=r=128,
         # 64 tokens/page, 512 logical pages per sequence, 65536 pages per plane.
