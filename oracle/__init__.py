@@ -90,6 +90,12 @@ def _load():
     lib.ropekv_oracle_paged_rows.restype = I
     lib.ropekv_oracle_paged.argtypes = [P] * 7 + [I] * 9
     lib.ropekv_oracle_paged.restype = I
+    lib.ropekv_oracle_delta_metadata.argtypes = [P, P, I, P, P, I]
+    lib.ropekv_oracle_delta_metadata.restype = I
+    lib.ropekv_oracle_gather_delta_rope.argtypes = [P, P, P, P, P, I, I, I, I, I]
+    lib.ropekv_oracle_gather_delta_rope.restype = I
+    lib.ropekv_oracle_paged_fused.argtypes = [P] * 9 + [I] * 10
+    lib.ropekv_oracle_paged_fused.restype = I
     lib.ropekv_oracle_capacity_rejected.argtypes = [ctypes.c_int32, ctypes.c_int32]
     lib.ropekv_oracle_capacity_rejected.restype = I
     _lib = lib
@@ -238,6 +244,51 @@ def paged(k_delta, v_delta, kv_pool, cos_sin_rows, delta_positions, delta_to_seq
         _ptr(delta_to_seq, np.int32), _ptr(page_table, np.int32),
         N, B, Hkv, D, r, num_pages, mpps, tpp, style)
     _check(rc, "paged")
+
+
+def delta_metadata(old_lengths, delta_lengths, delta_width):
+    """Returns (delta_positions, delta_token_to_sequence), each [B * delta_width] int32."""
+    old_lengths = np.ascontiguousarray(old_lengths, dtype=np.int32)
+    delta_lengths = np.ascontiguousarray(delta_lengths, dtype=np.int32)
+    B = old_lengths.shape[0]
+    pos = np.empty(B * delta_width, dtype=np.int32)
+    seq = np.empty(B * delta_width, dtype=np.int32)
+    rc = _load().ropekv_oracle_delta_metadata(_ptr(old_lengths, np.int32), _ptr(delta_lengths, np.int32),
+                                              delta_width, _ptr(pos, np.int32), _ptr(seq, np.int32), B)
+    _check(rc, "delta_metadata")
+    return pos, seq
+
+
+def gather_delta_rope(source, delta_positions, delta_to_seq, state_indices, batch_size):
+    """source [sourceRows, cacheCapacity, r] float32 -> [N, r] float32."""
+    source = np.ascontiguousarray(source, dtype=np.float32)
+    rows, cap, r = source.shape
+    N = delta_positions.shape[0]
+    out = np.full((N, r), np.nan, dtype=np.float32)
+    st = ctypes.c_void_p(0) if state_indices is None else _ptr(state_indices, np.int32)
+    rc = _load().ropekv_oracle_gather_delta_rope(_ptr(source, np.float32), _ptr(out, np.float32),
+                                                 _ptr(delta_positions, np.int32),
+                                                 _ptr(delta_to_seq, np.int32), st, N, batch_size,
+                                                 rows, cap, r)
+    _check(rc, "gather_delta_rope")
+    return out
+
+
+def paged_fused(k_delta, v_delta, kv_pool, source, old_lengths, delta_lengths, delta_width,
+                state_indices, page_table, style):
+    """The metadata + gather + paged update composition into a host pool (mutated)."""
+    N, Hkv, D = k_delta.shape
+    rows, cap, r = source.shape
+    B, two, mpps = page_table.shape
+    _, num_pages, tpp, hk2, d2 = kv_pool.shape
+    assert N == B * delta_width and two == 2 and hk2 == Hkv and d2 == D
+    st = ctypes.c_void_p(0) if state_indices is None else _ptr(state_indices, np.int32)
+    rc = _load().ropekv_oracle_paged_fused(
+        _ptr(k_delta, np.uint16), _ptr(v_delta, np.uint16), _ptr(kv_pool, np.uint16),
+        _ptr(source, np.float32), _ptr(np.ascontiguousarray(old_lengths, dtype=np.int32), np.int32),
+        _ptr(np.ascontiguousarray(delta_lengths, dtype=np.int32), np.int32), delta_width, st,
+        _ptr(page_table, np.int32), B, Hkv, D, r, num_pages, mpps, tpp, rows, cap, style)
+    _check(rc, "paged_fused")
 
 
 def capacity_rejected(cos_sin_seq_len: int, kv_capacity: int) -> bool:

@@ -339,6 +339,89 @@ int ropekv_oracle_paged(const uint16_t* kDelta, const uint16_t* vDelta, uint16_t
     return rc;
 }
 
+int ropekv_oracle_delta_metadata(const int32_t* oldDraftCacheLengths, const int32_t* deltaLengths,
+                                 int deltaWidth, int32_t* deltaPositions,
+                                 int32_t* deltaTokenToSequence, int batchSize)
+{
+    if (deltaWidth < 0 || batchSize < 0)
+        return -1;
+    for (int b = 0; b < batchSize; ++b) {
+        int len = deltaLengths[b]; /* rows past deltaWidth do not exist */
+        for (int j = 0; j < deltaWidth; ++j) {
+            size_t t = (size_t)b * deltaWidth + j;
+            if (j < len) {
+                /* the target length after the delta is old + len; the delta's
+                 * own tokens sit at old .. old + len - 1 */
+                deltaPositions[t] = oldDraftCacheLengths[b] + j;
+                deltaTokenToSequence[t] = b;
+            } else {
+                deltaPositions[t] = -1;
+                deltaTokenToSequence[t] = -1;
+            }
+        }
+    }
+    return 0;
+}
+
+int ropekv_oracle_gather_delta_rope(const float* source, float* output,
+                                    const int32_t* deltaPositions,
+                                    const int32_t* deltaTokenToSequence,
+                                    const int32_t* stateIndices, int numDeltaTokens,
+                                    int batchSize, int sourceRows, int cacheCapacity,
+                                    int rotaryDim)
+{
+    if (numDeltaTokens < 0 || batchSize < 0 || sourceRows < 0 || cacheCapacity < 0 ||
+        rotaryDim <= 0)
+        return -1;
+    for (int t = 0; t < numDeltaTokens; ++t) {
+        float* out = output + (size_t)t * rotaryDim;
+        int32_t pos = deltaPositions[t];
+        int32_t seq = deltaTokenToSequence[t];
+        int ok = pos >= 0 && seq >= 0 && seq < batchSize && pos < cacheCapacity;
+        int32_t state = -1;
+        if (ok) {
+            if (stateIndices != NULL)
+                state = stateIndices[seq];
+            else
+                state = (sourceRows == 1) ? 0 : seq;
+            ok = state >= 0 && state < sourceRows;
+        }
+        for (int d = 0; d < rotaryDim; ++d)
+            out[d] = ok ? source[((size_t)state * cacheCapacity + pos) * rotaryDim + d] : 0.0f;
+    }
+    return 0;
+}
+
+int ropekv_oracle_paged_fused(const uint16_t* kDelta, const uint16_t* vDelta, uint16_t* kvCache,
+                              const float* source, const int32_t* oldDraftCacheLengths,
+                              const int32_t* deltaLengths, int deltaWidth,
+                              const int32_t* stateIndices, const int32_t* pageTable,
+                              int batchSize, int Hkv, int D, int r, int numPages,
+                              int maxPagesPerSeq, int tokensPerPage, int sourceRows,
+                              int cacheCapacity, int style)
+{
+    if (batchSize < 0 || deltaWidth < 0 || r <= 0)
+        return -1;
+    size_t n = (size_t)batchSize * (size_t)deltaWidth;
+    size_t nn = n > 0 ? n : 1;
+    int32_t* pos = (int32_t*)malloc(sizeof(int32_t) * nn);
+    int32_t* seq = (int32_t*)malloc(sizeof(int32_t) * nn);
+    float* cs = (float*)calloc(nn * (size_t)r, sizeof(float));
+    int rc = ropekv_oracle_delta_metadata(oldDraftCacheLengths, deltaLengths, deltaWidth, pos, seq,
+                                          batchSize);
+    if (rc == 0)
+        rc = ropekv_oracle_gather_delta_rope(source, cs, pos, seq, stateIndices, (int)n,
+                                             batchSize, sourceRows, cacheCapacity, r);
+    if (rc == 0)
+        rc = ropekv_oracle_paged(kDelta, vDelta, kvCache, cs, pos, seq, pageTable, (int)n,
+                                 batchSize, Hkv, D, r, numPages, maxPagesPerSeq, tokensPerPage,
+                                 style);
+    free(cs);
+    free(seq);
+    free(pos);
+    return rc;
+}
+
 int ropekv_oracle_capacity_rejected(int32_t cosSinSeqLen, int32_t kvCapacity)
 {
     /* the RoPE table may be shorter than the page-aligned capacity; only a

@@ -15,7 +15,9 @@
  *         _get_neox_rotated_x, _get_gptj_rotated_x, _unit_rope, _load_cos_sin,
  *         kernel Stage 2.1 (frequency index) and the wrapper's cos_sin width rule.
  *   [DRK] TensorRT-Edge-LLM C++ API, "Dflash Runtime Kernels":
- *         launchDFlashTargetKVCacheUpdate, checkDFlashRopeCapacity.
+ *         launchDFlashTargetKVCacheUpdate, checkDFlashRopeCapacity,
+ *         launchDFlashPrepareDeltaMetadata, launchDFlashGatherDeltaRope,
+ *         launchDFlashPrepareProposalInputs (target length after the delta).
  *
  * Conventions shared by every function below:
  *   - FP16 tensors are passed as uint16_t arrays of IEEE 754 binary16 bits.
@@ -108,6 +110,43 @@ int ropekv_oracle_paged(const uint16_t* kDelta, const uint16_t* vDelta, uint16_t
                         const int32_t* pageTable,
                         int numDeltaTokens, int batchSize, int Hkv, int D, int r,
                         int numPages, int maxPagesPerSeq, int tokensPerPage, int style);
+
+/* [DRK] launchDFlashPrepareDeltaMetadata (the page gives the signature only).
+ * Reading: delta rows are laid out [batchSize, deltaWidth]; row b*deltaWidth + j
+ * is sequence b's j-th new token when j < deltaLengths[b] (a negative length
+ * counts as 0): position oldDraftCacheLengths[b] + j (the draft cache
+ * length before the delta, plus the offset inside the delta), sequence b.
+ * Every other row is padding: position -1, sequence -1. Writes
+ * batchSize*deltaWidth entries of each output. */
+int ropekv_oracle_delta_metadata(const int32_t* oldDraftCacheLengths, const int32_t* deltaLengths,
+                                 int deltaWidth, int32_t* deltaPositions,
+                                 int32_t* deltaTokenToSequence, int batchSize);
+
+/* [DRK] launchDFlashGatherDeltaRope (the page gives the signature only).
+ * Reading: source is a FP32 cos/sin cache [sourceRows, cacheCapacity, rotaryDim];
+ * output [numDeltaTokens, rotaryDim] is the token-aligned table of the paged
+ * update. Row t takes pos = deltaPositions[t], seq = deltaTokenToSequence[t] and
+ * the source row state = stateIndices[seq] (or, without stateIndices, 0 when
+ * sourceRows == 1, else seq); it copies source[state, pos, :] and is zero when
+ * pos < 0, seq < 0, seq >= batchSize, pos >= cacheCapacity or state is outside
+ * [0, sourceRows). stateIndices may be NULL. */
+int ropekv_oracle_gather_delta_rope(const float* source, float* output,
+                                    const int32_t* deltaPositions,
+                                    const int32_t* deltaTokenToSequence,
+                                    const int32_t* stateIndices, int numDeltaTokens,
+                                    int batchSize, int sourceRows, int cacheCapacity,
+                                    int rotaryDim);
+
+/* The DFlash target-KV step as one call: delta metadata, the cos/sin gather and
+ * the paged update above, in that order, on batchSize*deltaWidth delta rows.
+ * Defined as exactly that composition (scratch arrays are the oracle's own). */
+int ropekv_oracle_paged_fused(const uint16_t* kDelta, const uint16_t* vDelta, uint16_t* kvCache,
+                              const float* source, const int32_t* oldDraftCacheLengths,
+                              const int32_t* deltaLengths, int deltaWidth,
+                              const int32_t* stateIndices, const int32_t* pageTable,
+                              int batchSize, int Hkv, int D, int r, int numPages,
+                              int maxPagesPerSeq, int tokensPerPage, int sourceRows,
+                              int cacheCapacity, int style);
 
 /* [DRK] checkDFlashRopeCapacity: 1 when the pair is rejected
  * (cosSinSeqLen > kvCapacity), else 0. */

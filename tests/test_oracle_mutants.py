@@ -18,7 +18,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "ropekv_oracle.c")
 HDR = os.path.join(ROOT, "oracle", "ropekv_oracle.h")
 PIN_TESTS = ["tests/test_oracle_rope.py", "tests/test_oracle_entries.py",
-             "tests/test_oracle_fp16.py"]
+             "tests/test_oracle_dflash.py", "tests/test_oracle_fp16.py"]
 
 MUTANTS = {
     "neox_rotate_sign": ("out[d] = (d < h) ? -x[d + h] : x[d - h];",
@@ -51,6 +51,13 @@ MUTANTS = {
     "paged_capacity_unchecked": ("if (lp >= maxPagesPerSeq)", "if (lp > maxPagesPerSeq)"),
     "capacity_rule_inclusive": ("return cosSinSeqLen > kvCapacity ? 1 : 0;",
                                 "return cosSinSeqLen >= kvCapacity ? 1 : 0;"),
+    "metadata_position_base": ("deltaPositions[t] = oldDraftCacheLengths[b] + j;",
+                               "deltaPositions[t] = oldDraftCacheLengths[b] + j + 1;"),
+    "metadata_length_off_by_one": ("if (j < len) {", "if (j <= len) {"),
+    "gather_state_ignored": ("state = stateIndices[seq];", "state = seq;"),
+    "gather_capacity_unchecked": ("seq < batchSize && pos < cacheCapacity;",
+                                  "seq < batchSize && pos <= cacheCapacity;"),
+    "gather_shared_row_ignored": ("state = (sourceRows == 1) ? 0 : seq;", "state = seq;"),
 }
 
 
