@@ -40,7 +40,7 @@ import workloads  # noqa: E402
 
 METRIC = "fused RoPE+KV-write tokens/s and effective HBM GB/s (% of GB300 peak)"
 HEADLINE = "prefill"
-EXTRA = ("decode", "tree", "paged", "packed_tiny")
+EXTRA = ("decode", "tree", "paged", "packed_tiny", "paged_fused", "paged_fused_3launch")
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 
@@ -54,12 +54,30 @@ DESCR = {
             "depth 0..6, base in [128,4000], capacity 4096",
     "paged": "paged delta update: 16384 rows (15565 valid) over B=128, Hkv=8 D=r=128 NeoX, "
              "64 tokens/page, 512 pages/seq, 65536 pages per plane, 2% unmapped",
+    "paged_fused": "DFlash step in one launch (delta metadata + cos/sin gather + paged update): "
+                   "B=128 x deltaWidth 128 rows, lengths in [1,128], Hkv=8 D=r=128 NeoX, "
+                   "64 tokens/page, 512 pages/seq, 65536 pages per plane",
+    "paged_fused_3launch": "the same DFlash step as three launches (metadata, gather, update)",
     "decode_c1024": "decode as above with cache capacity 1024 (profiler-sized twin)",
     "paged_p8192": "paged as above with 64 pages/seq and 8192 pages per plane (profiler-sized twin)",
 }
 
 
 # ------------------------------------------------------------------ utils --
+
+def max_over_ranks(value: float, dist, device) -> float:
+    """Largest value over all ranks (the slowest rank's time)."""
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world: int, units_per_rank: int, steps: int, max_seconds: float) -> float:
+    """Weak scaling: every rank processes its own replica of the workload, so
+    the job's rate is all ranks' units over the slowest rank's time."""
+    return world * units_per_rank * steps / max_seconds
+
 
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -165,15 +183,16 @@ class DeviceWorkload:
         self.rk = rk
         self.name = name
         self.device = device
-        self.case = workloads.config(name)
+        self.three_launch = name.endswith("_3launch")
+        self.case = workloads.config(name[: -len("_3launch")] if self.three_launch else name)
         self.paged = isinstance(self.case, workloads.PagedCase)
+        self.fused = isinstance(self.case, workloads.PagedFusedCase)
         c = self.case
-        if self.paged:
+        if self.paged or self.fused:
             self.tokens = c.valid_rows
-            self.bytes = c.algorithmic_bytes()
         else:
             self.tokens = c.tokens
-            self.bytes = c.algorithmic_bytes()
+        self.bytes = c.algorithmic_bytes()
         self.ring = max(2, min(96, math.ceil(2 * l2_bytes / max(self.bytes, 1))))
         t = lambda a: self._dev(a)
         self.sets = []
@@ -186,7 +205,24 @@ class DeviceWorkload:
                 self.sets.append(dict(k=k_base.clone() if k else k_base,
                                       v=v_base.clone() if k else v_base,
                                       cs=cs.clone() if k else cs, pos=pos, seq=seq, pt=pt))
-            self.bytes = int(np.mean([self._paged_bytes(k) for k in range(self.ring)]))
+            self.bytes = int(np.mean([self._variant_bytes(k) for k in range(self.ring)]))
+        elif self.fused:
+            self.pool = self._sentinel(c.pool_shape())
+            self.source = t(c.source)
+            self.lens = t(c.delta_lengths)
+            self.state = t(c.state) if c.state is not None else None
+            k_base, v_base = t(c.k_delta), t(c.v_delta)
+            for k in range(self.ring):
+                old, pt = workloads.step_variant(c, k)
+                st = dict(k=k_base.clone() if k else k_base, v=v_base.clone() if k else v_base,
+                          old=t(old), pt=t(pt))
+                if self.three_launch:
+                    # the pipeline's intermediate arrays (owned by the caller)
+                    st["pos"] = torch.empty(c.N, dtype=torch.int32, device=device)
+                    st["seq"] = torch.empty(c.N, dtype=torch.int32, device=device)
+                    st["cs"] = torch.empty((c.N, c.r), dtype=torch.float32, device=device)
+                self.sets.append(st)
+            self.bytes = int(np.mean([self._variant_bytes(k) for k in range(self.ring)]))
         else:
             self.cos_sin = t(c.cos_sin)
             self.cache = (t(c.new_cache()) if c.cache_init == "zero"
@@ -214,21 +250,38 @@ class DeviceWorkload:
         return torch.full(shape, workloads.SENTINEL, dtype=torch.int16,
                           device=self.device).view(torch.float16)
 
-    def _paged_bytes(self, k):
+    def _variant_bytes(self, k):
         c = self.case
-        saved = c.page_table
-        c.page_table = workloads.step_variant(c, k)
+        saved = (c.page_table, getattr(c, "old_lengths", None))
+        v = workloads.step_variant(c, k)
+        if self.fused:
+            c.old_lengths, c.page_table = v
+        else:
+            c.page_table = v
         try:
             return c.algorithmic_bytes()
         finally:
-            c.page_table = saved
+            c.page_table = saved[0]
+            if self.fused:
+                c.old_lengths = saved[1]
 
     def footprint(self):
         return self.ring * self.bytes
 
     def call(self, k: int, stream):
         c, s, rk = self.case, self.sets[k % self.ring], self.rk
-        if self.paged:
+        if self.fused and self.three_launch:
+            rk.dflash_prepare_delta_metadata(s["old"], self.lens, c.W, s["pos"], s["seq"],
+                                             stream=stream)
+            rk.dflash_gather_delta_rope(self.source, s["cs"], s["pos"], s["seq"], self.state,
+                                        batch_size=c.B, stream=stream)
+            rk.paged_kv_delta_update(s["k"], s["v"], self.pool, s["cs"], s["pos"], s["seq"],
+                                     s["pt"], style=c.style, stream=stream)
+        elif self.fused:
+            rk.paged_kv_delta_update_fused(s["k"], s["v"], self.pool, self.source, s["old"],
+                                           self.lens, s["pt"], self.state, style=c.style,
+                                           stream=stream)
+        elif self.paged:
             rk.paged_kv_delta_update(s["k"], s["v"], self.pool, s["cs"], s["pos"], s["seq"],
                                      s["pt"], style=c.style, stream=stream)
         elif c.mode == "packed":
@@ -457,7 +510,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=HEADLINE,
-                    choices=list(workloads.CONFIG_NAMES) + list(workloads.PROFILE_NAMES),
+                    choices=list(workloads.CONFIG_NAMES) + list(workloads.PROFILE_NAMES)
+                    + list(workloads.NEXT_NAMES),
                     help="workload of the headline line (default: the prefill)")
     ap.add_argument("--extra-steps", type=int, default=4000,
                     help="timed launches per extra workload (decode, tree, paged, packed_tiny)")
@@ -500,13 +554,11 @@ def main(argv=None):
     wl = DeviceWorkload(name, dev, l2)
     sec, t0, t1 = time_steps(wl, args.steps, args.warmup, stream, barrier)
     if world > 1:
-        t = torch.tensor([sec], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        sec = float(t.item())
+        sec = max_over_ranks(sec, dist, dev)
     launch_s = sec / args.steps
     achieved = wl.bytes / launch_s / 1e9
     clocks = sampler.summary(t0, t1) if sampler else None
-    e2e = e2e_contiguous(wl, args.e2e_steps) if not wl.paged else None
+    e2e = e2e_contiguous(wl, args.e2e_steps) if not (wl.paged or wl.fused) else None
     tokens, bytes_step, ring = wl.tokens, wl.bytes, wl.ring
     kernel = _kernel_name(wl)
     del wl
@@ -522,6 +574,7 @@ def main(argv=None):
             per = s_ / args.extra_steps
             gbs = w.bytes / per / 1e9
             extra[xname] = {"workload": DESCR[xname], "tokens_per_step": w.tokens,
+                            "launches_per_step": 3 if w.three_launch else 1,
                             "bytes_per_step": w.bytes, "ring": w.ring,
                             "us_per_launch": per * 1e6, "tokens_per_s": w.tokens / per,
                             "effective_gbs": gbs, "frac_of_measured_peak": gbs / peak,
@@ -540,7 +593,7 @@ def main(argv=None):
     cpu_tokens, cpu_sec, cpu_calls, cpu_n = oracle_sample(args.cpu_seconds)
     line = {
         "metric": METRIC,
-        "value": world * tokens * args.steps / sec,
+        "value": whole_job_rate(world, tokens, args.steps, sec),
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -579,6 +632,10 @@ def main(argv=None):
 
 def _kernel_name(wl) -> str:
     c = wl.case
+    if wl.fused:
+        if wl.three_launch:
+            return "delta_metadata_kernel + gather_delta_rope_kernel + paged_delta_kernel"
+        return f"paged_delta_kernel<D={c.D}, {'NeoX' if c.style == 0 else 'GPT-J'}, fused>"
     if wl.paged:
         return f"paged_delta_kernel<D={c.D}, {'NeoX' if c.style == 0 else 'GPT-J'}>"
     return (f"rope_kv_token_kernel<D={c.D}, {'NeoX' if c.style == 0 else 'GPT-J'}, "

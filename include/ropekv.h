@@ -11,7 +11,8 @@
  *         (launchApplyRopeWriteKVPackedQKV, launchApplyRopeWriteKVContinuousQAndKVCache,
  *         launchApplyRopeWriteKVTreeDecoding).
  *   [DRK] TensorRT-Edge-LLM C++ API, "Dflash Runtime Kernels"
- *         (launchDFlashTargetKVCacheUpdate, checkDFlashRopeCapacity).
+ *         (launchDFlashTargetKVCacheUpdate, checkDFlashRopeCapacity,
+ *         launchDFlashPrepareDeltaMetadata, launchDFlashGatherDeltaRope).
  *   [RC]  sglang rope_cache.py (_get_neox_rotated_x, _get_gptj_rotated_x,
  *         _unit_rope, _load_cos_sin, kernel Stage 2.1).
  *
@@ -163,6 +164,76 @@ ROPEKV_API int paged_kv_delta_update(const uint16_t* kDelta, const uint16_t* vDe
                                      int32_t rotaryDim, int32_t numPages,
                                      int32_t maxPagesPerSeq, int32_t tokensPerPage,
                                      int32_t style, void* stream);
+
+/*
+ * The DFlash target-KV step as ONE launch: launchDFlashPrepareDeltaMetadata,
+ * launchDFlashGatherDeltaRope and launchDFlashTargetKVCacheUpdate of [DRK]
+ * folded together, so the per-row positions, sequences and cos/sin rows never
+ * go through memory. The result is exactly that of calling
+ * dflash_prepare_delta_metadata, dflash_gather_delta_rope and
+ * paged_kv_delta_update in that order on the same arguments.
+ *   kDelta, vDelta         [batchSize * deltaWidth, numKVHeads, headDim] FP16: row
+ *                          b * deltaWidth + j is sequence b's delta token j.
+ *   kvCache, pageTable     as paged_kv_delta_update.
+ *   cosSinSource           [sourceRows, cacheCapacity, rotaryDim] FP32 cos/sin cache.
+ *   oldDraftCacheLengths   [batchSize] INT32, draft cache lengths before the delta.
+ *   deltaLengths           [batchSize] INT32, delta tokens of each sequence; rows
+ *                          j >= deltaLengths[b] are padding.
+ *   stateIndices           [batchSize] INT32 source row of each sequence, or NULL
+ *                          (then row 0 when sourceRows == 1, else row b).
+ * Token j of sequence b sits at position oldDraftCacheLengths[b] + j. When its
+ * position is >= cacheCapacity or its source row is outside [0, sourceRows) the
+ * gather yields a zero cos/sin row, so rotated K dims are written as zeros.
+ * Host errors: as paged_kv_delta_update; deltaWidth, sourceRows or
+ * cacheCapacity negative, or batchSize * deltaWidth >= 2^31 -> ROPEKV_ERR_SHAPE.
+ */
+ROPEKV_API int paged_kv_delta_update_fused(const uint16_t* kDelta, const uint16_t* vDelta,
+                                           uint16_t* kvCache, const float* cosSinSource,
+                                           const int32_t* oldDraftCacheLengths,
+                                           const int32_t* deltaLengths, int32_t deltaWidth,
+                                           const int32_t* stateIndices, const int32_t* pageTable,
+                                           int32_t batchSize, int32_t numKVHeads,
+                                           int32_t headDim, int32_t rotaryDim, int32_t numPages,
+                                           int32_t maxPagesPerSeq, int32_t tokensPerPage,
+                                           int32_t sourceRows, int32_t cacheCapacity,
+                                           int32_t style, void* stream);
+
+/*
+ * [DRK] launchDFlashPrepareDeltaMetadata (the page prints only the signature).
+ * Reading used here: delta rows are laid out [batchSize, deltaWidth]; row
+ * t = b * deltaWidth + j gets deltaPositions[t] = oldDraftCacheLengths[b] + j and
+ * deltaTokenToSequence[t] = b when j < deltaLengths[b], else -1 and -1 (padding).
+ * (The target length after the delta is oldDraftCacheLengths[b] + deltaLength,
+ * as [DRK] launchDFlashPrepareProposalInputs states.)
+ *   oldDraftCacheLengths, deltaLengths  [batchSize] INT32, read.
+ *   deltaPositions, deltaTokenToSequence [batchSize * deltaWidth] INT32, written.
+ * Host errors: negative sizes or batchSize * deltaWidth >= 2^31 -> ROPEKV_ERR_SHAPE.
+ */
+ROPEKV_API int dflash_prepare_delta_metadata(const int32_t* oldDraftCacheLengths,
+                                             const int32_t* deltaLengths, int32_t deltaWidth,
+                                             int32_t* deltaPositions,
+                                             int32_t* deltaTokenToSequence, int32_t batchSize,
+                                             void* stream);
+
+/*
+ * [DRK] launchDFlashGatherDeltaRope (the page prints only the signature).
+ * Reading used here: output row t is the tokenAlignedCosSin row of delta row t,
+ *   output[t, :] = source[state, deltaPositions[t], :],
+ * with state = stateIndices[seq] (stateIndices may be NULL: then 0 when
+ * sourceRows == 1, else seq) and seq = deltaTokenToSequence[t]; the row is zero
+ * when the position is negative or >= cacheCapacity, seq is negative or
+ * >= batchSize, or state is outside [0, sourceRows).
+ *   source  [sourceRows, cacheCapacity, rotaryDim] FP32, read.
+ *   output  [numDeltaTokens, rotaryDim] FP32, written (every row).
+ * Host errors: rotaryDim not a multiple of 16 in [16, 256] -> ROPEKV_ERR_ROTARY_DIM;
+ * negative sizes -> ROPEKV_ERR_SHAPE.
+ */
+ROPEKV_API int dflash_gather_delta_rope(const float* source, float* output,
+                                        const int32_t* deltaPositions,
+                                        const int32_t* deltaTokenToSequence,
+                                        const int32_t* stateIndices, int32_t numDeltaTokens,
+                                        int32_t batchSize, int32_t sourceRows,
+                                        int32_t cacheCapacity, int32_t rotaryDim, void* stream);
 
 /*
  * [DRK] checkDFlashRopeCapacity: the RoPE table must cover every position the

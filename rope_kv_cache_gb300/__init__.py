@@ -9,9 +9,12 @@ from ._binding import (  # noqa: F401
     NEOX,
     LIB_PATH,
     RopeKVError,
+    dflash_gather_delta_rope,
+    dflash_prepare_delta_metadata,
     library_path,
     load_library,
     paged_kv_delta_update,
+    paged_kv_delta_update_fused,
     rope_check_capacity,
     rope_write_kv_continuous,
     rope_write_kv_packed,
@@ -22,5 +25,6 @@ from ._binding import (  # noqa: F401
 __all__ = [
     "NEOX", "GPTJ", "RopeKVError", "load_library", "library_path",
     "rope_write_kv_packed", "rope_write_kv_continuous", "rope_write_kv_tree",
-    "paged_kv_delta_update", "rope_check_capacity", "ropekv_status_string",
+    "paged_kv_delta_update", "paged_kv_delta_update_fused", "dflash_prepare_delta_metadata",
+    "dflash_gather_delta_rope", "rope_check_capacity", "ropekv_status_string",
 ]

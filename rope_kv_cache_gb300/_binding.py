@@ -60,11 +60,15 @@ def load_library():
     lib.rope_write_kv_continuous.argtypes = [P, P, P, P, P, D, P]
     lib.rope_write_kv_tree.argtypes = [P, P, P, P, P, P, D, P]
     lib.paged_kv_delta_update.argtypes = [P] * 7 + [I32] * 9 + [P]
+    lib.paged_kv_delta_update_fused.argtypes = [P] * 6 + [I32] + [P] * 2 + [I32] * 10 + [P]
+    lib.dflash_prepare_delta_metadata.argtypes = [P, P, I32, P, P, I32, P]
+    lib.dflash_gather_delta_rope.argtypes = [P] * 5 + [I32] * 5 + [P]
     lib.rope_check_capacity.argtypes = [I32, I32]
     lib.ropekv_status_string.argtypes = [ctypes.c_int]
     lib.ropekv_status_string.restype = ctypes.c_char_p
     for fn in ("rope_write_kv_packed", "rope_write_kv_continuous", "rope_write_kv_tree",
-               "paged_kv_delta_update", "rope_check_capacity"):
+               "paged_kv_delta_update", "paged_kv_delta_update_fused",
+               "dflash_prepare_delta_metadata", "dflash_gather_delta_rope", "rope_check_capacity"):
         getattr(lib, fn).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -221,3 +225,91 @@ def paged_kv_delta_update(k_delta: torch.Tensor, v_delta: torch.Tensor, kv_cache
         N, batch_size, Hkv, D, token_aligned_cos_sin.shape[1], num_pages, mpps, tpp, style,
         _stream_handle(stream, dev))
     _check_rc("paged_kv_delta_update", rc)
+
+
+def paged_kv_delta_update_fused(k_delta: torch.Tensor, v_delta: torch.Tensor,
+                                kv_cache: torch.Tensor, cos_sin_source: torch.Tensor,
+                                old_draft_cache_lengths: torch.Tensor,
+                                delta_lengths: torch.Tensor, page_table: torch.Tensor,
+                                state_indices: Optional[torch.Tensor] = None, style: int = NEOX,
+                                stream: Optional[torch.cuda.Stream] = None) -> None:
+    """DFlash metadata + cos/sin gather + paged update in one launch.
+
+    k_delta, v_delta [B * W, Hkv, D] float16 (row b*W + j = sequence b's token j);
+    kv_cache [2, numPages, tokensPerPage, Hkv, D] float16; cos_sin_source
+    [sourceRows, cacheCapacity, r] float32; old_draft_cache_lengths, delta_lengths
+    [B] int32; page_table [B, 2, maxPagesPerSeq] int32; state_indices [B] int32 or None.
+    """
+    if k_delta.dim() != 3 or kv_cache.dim() != 5 or page_table.dim() != 3 \
+            or cos_sin_source.dim() != 3:
+        raise ValueError("k_delta [B*W,Hkv,D], kv_cache [2,P,TPP,Hkv,D], page_table [B,2,M], "
+                         "cos_sin_source [rows,cap,r] expected")
+    N, Hkv, D = k_delta.shape
+    two, num_pages, tpp, hk2, d2 = kv_cache.shape
+    B, two_b, mpps = page_table.shape
+    rows, cap, r = cos_sin_source.shape
+    if B == 0 or N % B != 0:
+        raise ValueError("k_delta rows must be batch * deltaWidth")
+    width = N // B
+    if tuple(v_delta.shape) != (N, Hkv, D) or two != 2 or hk2 != Hkv or d2 != D or two_b != 2 \
+            or tuple(old_draft_cache_lengths.shape) != (B,) or tuple(delta_lengths.shape) != (B,) \
+            or (state_indices is not None and tuple(state_indices.shape) != (B,)):
+        raise ValueError("inconsistent shapes for paged_kv_delta_update_fused")
+    dev = k_delta.device
+    rc = load_library().paged_kv_delta_update_fused(
+        _dev_ptr(k_delta, "k_delta", _F16, dev), _dev_ptr(v_delta, "v_delta", _F16, dev),
+        _dev_ptr(kv_cache, "kv_cache", _F16, dev),
+        _dev_ptr(cos_sin_source, "cos_sin_source", _F32, dev),
+        _dev_ptr(old_draft_cache_lengths, "old_draft_cache_lengths", _I32, dev),
+        _dev_ptr(delta_lengths, "delta_lengths", _I32, dev), width,
+        _dev_ptr(state_indices, "state_indices", _I32, dev),
+        _dev_ptr(page_table, "page_table", _I32, dev),
+        B, Hkv, D, r, num_pages, mpps, tpp, rows, cap, style, _stream_handle(stream, dev))
+    _check_rc("paged_kv_delta_update_fused", rc)
+
+
+def dflash_prepare_delta_metadata(old_draft_cache_lengths: torch.Tensor,
+                                  delta_lengths: torch.Tensor, delta_width: int,
+                                  delta_positions: torch.Tensor,
+                                  delta_token_to_sequence: torch.Tensor,
+                                  stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Rows [B, delta_width]: position old[b] + j and sequence b when j < delta_lengths[b],
+    else -1 / -1. Outputs are int32 tensors of B * delta_width elements."""
+    B = old_draft_cache_lengths.shape[0]
+    if tuple(delta_lengths.shape) != (B,) or delta_positions.numel() != B * delta_width \
+            or delta_token_to_sequence.numel() != B * delta_width:
+        raise ValueError("inconsistent shapes for dflash_prepare_delta_metadata")
+    dev = old_draft_cache_lengths.device
+    rc = load_library().dflash_prepare_delta_metadata(
+        _dev_ptr(old_draft_cache_lengths, "old_draft_cache_lengths", _I32, dev),
+        _dev_ptr(delta_lengths, "delta_lengths", _I32, dev), int(delta_width),
+        _dev_ptr(delta_positions, "delta_positions", _I32, dev),
+        _dev_ptr(delta_token_to_sequence, "delta_token_to_sequence", _I32, dev), B,
+        _stream_handle(stream, dev))
+    _check_rc("dflash_prepare_delta_metadata", rc)
+
+
+def dflash_gather_delta_rope(source: torch.Tensor, output: torch.Tensor,
+                             delta_positions: torch.Tensor, delta_token_to_sequence: torch.Tensor,
+                             state_indices: Optional[torch.Tensor] = None,
+                             batch_size: Optional[int] = None,
+                             stream: Optional[torch.cuda.Stream] = None) -> None:
+    """output[t] = source[state(seq_t), pos_t] (zero rows where out of range).
+    source [sourceRows, cacheCapacity, r] float32; output [N, r] float32;
+    batch_size defaults to len(state_indices) when given, else to N."""
+    if source.dim() != 3 or output.dim() != 2:
+        raise ValueError("source [rows,cap,r] and output [N,r] expected")
+    rows, cap, r = source.shape
+    N = output.shape[0]
+    if output.shape[1] != r or delta_positions.numel() != N or delta_token_to_sequence.numel() != N:
+        raise ValueError("inconsistent shapes for dflash_gather_delta_rope")
+    if batch_size is None:
+        batch_size = state_indices.shape[0] if state_indices is not None else N
+    dev = output.device
+    rc = load_library().dflash_gather_delta_rope(
+        _dev_ptr(source, "source", _F32, dev), _dev_ptr(output, "output", _F32, dev),
+        _dev_ptr(delta_positions, "delta_positions", _I32, dev),
+        _dev_ptr(delta_token_to_sequence, "delta_token_to_sequence", _I32, dev),
+        _dev_ptr(state_indices, "state_indices", _I32, dev), N, int(batch_size), rows, cap, r,
+        _stream_handle(stream, dev))
+    _check_rc("dflash_gather_delta_rope", rc)

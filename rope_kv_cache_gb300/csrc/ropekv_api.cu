@@ -19,6 +19,11 @@ bool aligned16(const void* p)
     return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
 }
 
+int launch_status()
+{
+    return cudaGetLastError() == cudaSuccess ? ROPEKV_OK : ROPEKV_ERR_LAUNCH;
+}
+
 int check_head_dims(int32_t D, int32_t r)
 {
     if (D != 64 && D != 128 && D != 256)
@@ -103,29 +108,67 @@ void dispatch_token(const TokenArgs& a, int D, int style, long long tokens, cons
     }
 }
 
-template <int D, int STYLE>
+template <int D, int STYLE, bool FUSED>
 void launch_paged(const PagedArgs& a, long long rows, const Shape& sh, cudaStream_t st)
 {
     const unsigned grid = (unsigned)(rows * sh.ctasPerUnit);
     if (sh.ipt == 2)
-        ropekv::paged_delta_kernel<D, STYLE, 2, kPolicy><<<grid, sh.threads, 0, st>>>(a);
+        ropekv::paged_delta_kernel<D, STYLE, 2, kPolicy, FUSED><<<grid, sh.threads, 0, st>>>(a);
     else
-        ropekv::paged_delta_kernel<D, STYLE, 1, kPolicy><<<grid, sh.threads, 0, st>>>(a);
+        ropekv::paged_delta_kernel<D, STYLE, 1, kPolicy, FUSED><<<grid, sh.threads, 0, st>>>(a);
 }
 
-template <int D>
-void dispatch_paged_style(const PagedArgs& a, int style, long long rows, const Shape& sh,
-                          cudaStream_t st)
+template <bool FUSED>
+void dispatch_paged(const PagedArgs& a, int D, int style, long long rows, const Shape& sh,
+                    cudaStream_t st)
 {
-    if (style == ROPEKV_GPTJ)
-        launch_paged<D, ropekv::kGptj>(a, rows, sh, st);
-    else
-        launch_paged<D, ropekv::kNeox>(a, rows, sh, st);
+    const bool gptj = style == ROPEKV_GPTJ;
+    switch (D) {
+    case 64:
+        gptj ? launch_paged<64, ropekv::kGptj, FUSED>(a, rows, sh, st)
+             : launch_paged<64, ropekv::kNeox, FUSED>(a, rows, sh, st);
+        break;
+    case 128:
+        gptj ? launch_paged<128, ropekv::kGptj, FUSED>(a, rows, sh, st)
+             : launch_paged<128, ropekv::kNeox, FUSED>(a, rows, sh, st);
+        break;
+    default:
+        gptj ? launch_paged<256, ropekv::kGptj, FUSED>(a, rows, sh, st)
+             : launch_paged<256, ropekv::kNeox, FUSED>(a, rows, sh, st);
+        break;
+    }
 }
 
-int launch_status()
+// Checks shared by both paged calls (sizes and style).
+int check_paged_sizes(int32_t numRows, int32_t batchSize, int32_t numKVHeads, int32_t headDim,
+                      int32_t rotaryDim, int32_t numPages, int32_t maxPagesPerSeq,
+                      int32_t tokensPerPage, int32_t style)
 {
-    return cudaGetLastError() == cudaSuccess ? ROPEKV_OK : ROPEKV_ERR_LAUNCH;
+    if (style != ROPEKV_NEOX && style != ROPEKV_GPTJ)
+        return ROPEKV_ERR_STYLE;
+    int rc = check_head_dims(headDim, rotaryDim);
+    if (rc != ROPEKV_OK)
+        return rc;
+    if (numKVHeads <= 0)
+        return ROPEKV_ERR_HEADS;
+    if (numRows < 0 || batchSize < 0 || numPages < 0 || maxPagesPerSeq < 0 || tokensPerPage <= 0)
+        return ROPEKV_ERR_SHAPE;
+    if (2LL * numKVHeads * (headDim / 16) > (1LL << 30))
+        return ROPEKV_ERR_SHAPE;
+    return ROPEKV_OK;
+}
+
+int launch_paged_rows(PagedArgs& a, long long rows, int D, int style, bool fused, cudaStream_t st)
+{
+    const Shape sh = pick_shape(a.itemsPerRow, rows);
+    if (rows * sh.ctasPerUnit > 0x7FFFFFFFLL)
+        return ROPEKV_ERR_SHAPE;
+    a.ctasPerRow = sh.ctasPerUnit;
+    if (fused)
+        dispatch_paged<true>(a, D, style, rows, sh, st);
+    else
+        dispatch_paged<false>(a, D, style, rows, sh, st);
+    return launch_status();
 }
 
 // Checks shared by the three contiguous-cache calls. On success fills the
@@ -271,19 +314,10 @@ int paged_kv_delta_update(const uint16_t* kDelta, const uint16_t* vDelta, uint16
                           int32_t maxPagesPerSeq, int32_t tokensPerPage, int32_t style,
                           void* stream)
 {
-    if (style != ROPEKV_NEOX && style != ROPEKV_GPTJ)
-        return ROPEKV_ERR_STYLE;
-    int rc = check_head_dims(headDim, rotaryDim);
+    int rc = check_paged_sizes(numDeltaTokens, batchSize, numKVHeads, headDim, rotaryDim,
+                               numPages, maxPagesPerSeq, tokensPerPage, style);
     if (rc != ROPEKV_OK)
         return rc;
-    if (numKVHeads <= 0)
-        return ROPEKV_ERR_HEADS;
-    if (numDeltaTokens < 0 || batchSize < 0 || numPages < 0 || maxPagesPerSeq < 0 ||
-        tokensPerPage <= 0)
-        return ROPEKV_ERR_SHAPE;
-    const long long items = 2LL * numKVHeads * (headDim / 16);
-    if (items > (1LL << 30))
-        return ROPEKV_ERR_SHAPE;
     if (numDeltaTokens == 0)
         return ROPEKV_OK;
     if (!kDelta || !vDelta || !kvCache || !tokenAlignedCosSin || !deltaPositions ||
@@ -309,17 +343,105 @@ int paged_kv_delta_update(const uint16_t* kDelta, const uint16_t* vDelta, uint16
     a.numPages = numPages;
     a.mpps = maxPagesPerSeq;
     a.tpp = tokensPerPage;
-    a.itemsPerRow = (int32_t)items;
-    const Shape sh = pick_shape(a.itemsPerRow, numDeltaTokens);
-    if ((long long)numDeltaTokens * sh.ctasPerUnit > 0x7FFFFFFFLL)
+    a.itemsPerRow = 2 * numKVHeads * (headDim / 16);
+    return launch_paged_rows(a, numDeltaTokens, headDim, style, false, (cudaStream_t)stream);
+}
+
+int paged_kv_delta_update_fused(const uint16_t* kDelta, const uint16_t* vDelta,
+                                uint16_t* kvCache, const float* cosSinSource,
+                                const int32_t* oldDraftCacheLengths,
+                                const int32_t* deltaLengths, int32_t deltaWidth,
+                                const int32_t* stateIndices, const int32_t* pageTable,
+                                int32_t batchSize, int32_t numKVHeads, int32_t headDim,
+                                int32_t rotaryDim, int32_t numPages, int32_t maxPagesPerSeq,
+                                int32_t tokensPerPage, int32_t sourceRows,
+                                int32_t cacheCapacity, int32_t style, void* stream)
+{
+    if (deltaWidth < 0 || sourceRows < 0 || cacheCapacity < 0)
         return ROPEKV_ERR_SHAPE;
-    a.ctasPerRow = sh.ctasPerUnit;
-    cudaStream_t st = (cudaStream_t)stream;
-    switch (headDim) {
-    case 64: dispatch_paged_style<64>(a, style, numDeltaTokens, sh, st); break;
-    case 128: dispatch_paged_style<128>(a, style, numDeltaTokens, sh, st); break;
-    default: dispatch_paged_style<256>(a, style, numDeltaTokens, sh, st); break;
-    }
+    const long long rows = (long long)batchSize * deltaWidth;
+    if (rows > 0x7FFFFFFFLL)
+        return ROPEKV_ERR_SHAPE;
+    int rc = check_paged_sizes((int32_t)rows, batchSize, numKVHeads, headDim, rotaryDim,
+                               numPages, maxPagesPerSeq, tokensPerPage, style);
+    if (rc != ROPEKV_OK)
+        return rc;
+    if (rows == 0)
+        return ROPEKV_OK;
+    if (!kDelta || !vDelta || !kvCache || !cosSinSource || !oldDraftCacheLengths ||
+        !deltaLengths || !pageTable)
+        return ROPEKV_ERR_NULL_POINTER;
+    if (!aligned16(kDelta) || !aligned16(vDelta) || !aligned16(kvCache) ||
+        !aligned16(cosSinSource) || !aligned16(oldDraftCacheLengths) ||
+        !aligned16(deltaLengths) || !aligned16(stateIndices) || !aligned16(pageTable))
+        return ROPEKV_ERR_MISALIGNED;
+    PagedArgs a = {};
+    a.kDelta = kDelta;
+    a.vDelta = vDelta;
+    a.pool = kvCache;
+    a.cosSin = cosSinSource;
+    a.pageTable = pageTable;
+    a.oldLens = oldDraftCacheLengths;
+    a.deltaLens = deltaLengths;
+    a.stateIdx = stateIndices;
+    a.B = batchSize;
+    a.Hkv = numKVHeads;
+    a.r = rotaryDim;
+    a.numPages = numPages;
+    a.mpps = maxPagesPerSeq;
+    a.tpp = tokensPerPage;
+    a.deltaWidth = deltaWidth;
+    a.sourceRows = sourceRows;
+    a.cacheCapacity = cacheCapacity;
+    a.itemsPerRow = 2 * numKVHeads * (headDim / 16);
+    return launch_paged_rows(a, rows, headDim, style, true, (cudaStream_t)stream);
+}
+
+int dflash_prepare_delta_metadata(const int32_t* oldDraftCacheLengths,
+                                  const int32_t* deltaLengths, int32_t deltaWidth,
+                                  int32_t* deltaPositions, int32_t* deltaTokenToSequence,
+                                  int32_t batchSize, void* stream)
+{
+    if (deltaWidth < 0 || batchSize < 0)
+        return ROPEKV_ERR_SHAPE;
+    const long long rows = (long long)batchSize * deltaWidth;
+    if (rows > 0x7FFFFFFFLL)
+        return ROPEKV_ERR_SHAPE;
+    if (rows == 0)
+        return ROPEKV_OK;
+    if (!oldDraftCacheLengths || !deltaLengths || !deltaPositions || !deltaTokenToSequence)
+        return ROPEKV_ERR_NULL_POINTER;
+    if (!aligned16(oldDraftCacheLengths) || !aligned16(deltaLengths) ||
+        !aligned16(deltaPositions) || !aligned16(deltaTokenToSequence))
+        return ROPEKV_ERR_MISALIGNED;
+    ropekv::DeltaMetaArgs a = {oldDraftCacheLengths, deltaLengths, deltaPositions,
+                               deltaTokenToSequence, batchSize, deltaWidth};
+    const unsigned grid = (unsigned)((rows + 255) / 256);
+    ropekv::delta_metadata_kernel<<<grid, 256, 0, (cudaStream_t)stream>>>(a);
+    return launch_status();
+}
+
+int dflash_gather_delta_rope(const float* source, float* output, const int32_t* deltaPositions,
+                             const int32_t* deltaTokenToSequence, const int32_t* stateIndices,
+                             int32_t numDeltaTokens, int32_t batchSize, int32_t sourceRows,
+                             int32_t cacheCapacity, int32_t rotaryDim, void* stream)
+{
+    if (rotaryDim < 16 || rotaryDim > 256 || (rotaryDim % 16) != 0)
+        return ROPEKV_ERR_ROTARY_DIM;
+    if (numDeltaTokens < 0 || batchSize < 0 || sourceRows < 0 || cacheCapacity < 0)
+        return ROPEKV_ERR_SHAPE;
+    if (numDeltaTokens == 0)
+        return ROPEKV_OK;
+    if (!output || !deltaPositions || !deltaTokenToSequence || (!source && sourceRows > 0))
+        return ROPEKV_ERR_NULL_POINTER;
+    if (!aligned16(source) || !aligned16(output) || !aligned16(deltaPositions) ||
+        !aligned16(deltaTokenToSequence) || !aligned16(stateIndices))
+        return ROPEKV_ERR_MISALIGNED;
+    ropekv::GatherArgs a = {source, output, deltaPositions, deltaTokenToSequence, stateIndices,
+                            numDeltaTokens, batchSize, sourceRows, cacheCapacity, rotaryDim};
+    const long long n = (long long)numDeltaTokens * (rotaryDim / 4);
+    const unsigned grid = (unsigned)((n + 255) / 256);
+    ropekv::gather_delta_rope_kernel<<<grid, 256, 0, (cudaStream_t)stream>>>(a);
     return launch_status();
 }
 

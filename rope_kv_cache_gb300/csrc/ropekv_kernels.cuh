@@ -56,13 +56,35 @@ struct PagedArgs {
     const uint16_t* kDelta;    // [N, Hkv, D]
     const uint16_t* vDelta;    // [N, Hkv, D]
     uint16_t* pool;            // [2, numPages, tpp, Hkv, D]
-    const float* cosSin;       // [N, r] token-aligned
-    const int32_t* positions;  // [N]
-    const int32_t* seqIds;     // [N]
+    const float* cosSin;       // [N, r] token-aligned; fused: [sourceRows, cacheCapacity, r]
+    const int32_t* positions;  // [N]                 (explicit metadata)
+    const int32_t* seqIds;     // [N]                 (explicit metadata)
     const int32_t* pageTable;  // [B, 2, mpps]
+    const int32_t* oldLens;    // [B] draft cache lengths before the delta   (fused)
+    const int32_t* deltaLens;  // [B] delta tokens per sequence             (fused)
+    const int32_t* stateIdx;   // [B] cos/sin source row per sequence, or NULL (fused)
     int32_t B, Hkv, r, numPages, mpps, tpp;
+    int32_t deltaWidth, sourceRows, cacheCapacity;  // (fused)
     int32_t itemsPerRow;       // 2 * Hkv * D / 16 (K heads, then V heads)
     int32_t ctasPerRow;
+};
+
+// Arguments of the DFlash delta-metadata and cos/sin gather kernels.
+struct DeltaMetaArgs {
+    const int32_t* oldLens;    // [B]
+    const int32_t* deltaLens;  // [B]
+    int32_t* positions;        // [B * width]
+    int32_t* seqIds;           // [B * width]
+    int32_t B, width;
+};
+
+struct GatherArgs {
+    const float* source;       // [sourceRows, cacheCapacity, r]
+    float* output;             // [N, r]
+    const int32_t* positions;  // [N]
+    const int32_t* seqIds;     // [N]
+    const int32_t* stateIdx;   // [B] or NULL
+    int32_t N, B, sourceRows, cacheCapacity, r;
 };
 
 // --------------------------------------------------------------- helpers --
@@ -350,7 +372,17 @@ __global__ void __launch_bounds__(256) rope_kv_token_kernel(const TokenArgs a)
 //
 // Grid: rows * ctasPerRow CTAs; items [0, Hkv*D/16) are K heads, the rest V
 // heads, split across the CTAs of a row like the token kernel.
-template <int D, int STYLE, int IPT, int POL>
+//
+// FUSED = false: row t's position and sequence come from deltaPositions /
+// deltaTokenToSequence and its cos/sin from row t of the token-aligned table
+// ("Dflash Runtime Kernels", launchDFlashTargetKVCacheUpdate).
+// FUSED = true: the same update with the two preceding DFlash steps folded in
+// (launchDFlashPrepareDeltaMetadata, launchDFlashGatherDeltaRope): row
+// t = b * deltaWidth + j is sequence b's token j when j < deltaLens[b], at
+// position oldLens[b] + j, and its cos/sin row is read straight from the source
+// cache at (state row of b, position) -- a zero row when that is out of range,
+// exactly as the gather would have produced.
+template <int D, int STYLE, int IPT, int POL, bool FUSED>
 __global__ void __launch_bounds__(256) paged_delta_kernel(const PagedArgs a)
 {
     constexpr int kItemsPerHead = D / 16;
@@ -362,8 +394,17 @@ __global__ void __launch_bounds__(256) paged_delta_kernel(const PagedArgs a)
     const int item0 = part * blockDim.x * IPT + threadIdx.x;
     const int kItems = a.Hkv * kItemsPerHead;
 
-    const int pos = __ldg(a.positions + t);
-    const int seq = __ldg(a.seqIds + t);
+    int pos, seq;
+    if (FUSED) {
+        seq = t / a.deltaWidth;
+        const int j = t - seq * a.deltaWidth;
+        if (j >= __ldg(a.deltaLens + seq))
+            return;  // padding row of the [B, deltaWidth] layout
+        pos = __ldg(a.oldLens + seq) + j;
+    } else {
+        pos = __ldg(a.positions + t);
+        seq = __ldg(a.seqIds + t);
+    }
     if (pos < 0 || seq < 0 || seq >= a.B)
         return;  // padding row
     const int lp = pos / a.tpp;
@@ -397,8 +438,25 @@ __global__ void __launch_bounds__(256) paged_delta_kernel(const PagedArgs a)
 
     float c[8], sn[8];
     const bool rotItem = i < (a.r >> 4);
-    if (rotItem && kOk)
-        load_cos_sin<STYLE, POL>(a.cosSin + (size_t)t * a.r, i, a.r, c, sn, pol);
+    if (rotItem && kOk) {
+        if (FUSED) {
+            int state = -1;
+            if (pos < a.cacheCapacity)
+                state = a.stateIdx ? __ldg(a.stateIdx + seq) : (a.sourceRows == 1 ? 0 : seq);
+            if (state >= 0 && state < a.sourceRows) {
+                load_cos_sin<STYLE, POL>(a.cosSin + ((size_t)state * a.cacheCapacity + pos) * a.r,
+                                         i, a.r, c, sn, pol);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    c[k] = 0.0f;
+                    sn[k] = 0.0f;
+                }
+            }
+        } else {
+            load_cos_sin<STYLE, POL>(a.cosSin + (size_t)t * a.r, i, a.r, c, sn, pol);
+        }
+    }
 
     const size_t rowElems = (size_t)a.Hkv * D;
 #pragma unroll
@@ -417,6 +475,44 @@ __global__ void __launch_bounds__(256) paged_delta_kernel(const PagedArgs a)
         store_v<POL>(dst + 8 * va, xa[k], pol);
         store_v<POL>(dst + 8 * vb, xb[k], pol);
     }
+}
+
+// ------------------------------------------------- DFlash prologue kernels --
+//
+// "Dflash Runtime Kernels", launchDFlashPrepareDeltaMetadata (signature only on
+// the page; rows laid out [B, width]): one thread per row.
+__global__ void __launch_bounds__(256) delta_metadata_kernel(const DeltaMetaArgs a)
+{
+    const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= (long long)a.B * a.width)
+        return;
+    const int b = (int)(t / a.width);
+    const int j = (int)(t - (long long)b * a.width);
+    const bool valid = j < __ldg(a.deltaLens + b);
+    a.positions[t] = valid ? __ldg(a.oldLens + b) + j : -1;
+    a.seqIds[t] = valid ? b : -1;
+}
+
+// launchDFlashGatherDeltaRope (signature only on the page): one thread per
+// float4 of an output row; zero rows where the source has no row.
+__global__ void __launch_bounds__(256) gather_delta_rope_kernel(const GatherArgs a)
+{
+    const int q4 = a.r >> 2;
+    const long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (g >= (long long)a.N * q4)
+        return;
+    const int t = (int)(g / q4);
+    const int q = (int)(g - (long long)t * q4);
+    const int pos = __ldg(a.positions + t);
+    const int seq = __ldg(a.seqIds + t);
+    int state = -1;
+    if (pos >= 0 && seq >= 0 && seq < a.B && pos < a.cacheCapacity)
+        state = a.stateIdx ? __ldg(a.stateIdx + seq) : (a.sourceRows == 1 ? 0 : seq);
+    float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    if (state >= 0 && state < a.sourceRows)
+        v = __ldg(reinterpret_cast<const float4*>(
+                a.source + ((size_t)state * a.cacheCapacity + pos) * a.r) + q);
+    reinterpret_cast<float4*>(a.output + (size_t)t * a.r)[q] = v;
 }
 
 }  // namespace ropekv

@@ -38,7 +38,9 @@ def declared_symbols():
 def test_header_declares_the_entry_points():
     names = set(declared_symbols())
     assert names == {"rope_write_kv_packed", "rope_write_kv_continuous", "rope_write_kv_tree",
-                     "paged_kv_delta_update", "rope_check_capacity", "ropekv_status_string"}
+                     "paged_kv_delta_update", "paged_kv_delta_update_fused",
+                     "dflash_prepare_delta_metadata", "dflash_gather_delta_rope",
+                     "rope_check_capacity", "ropekv_status_string"}
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -134,3 +136,37 @@ def test_status_strings(lib):
         s = rk.ropekv_status_string(code)
         assert s and s != "unknown status"
     assert rk.ropekv_status_string(-99) == "unknown status"
+
+
+def _fused(lib, *, ptrs=None, W=16, B=4, Hkv=8, D=128, r=128, P=16, M=8, tpp=64, rows=1, cap=64,
+           style=0):
+    p = ptrs or [A] * 9
+    return lib.paged_kv_delta_update_fused(p[0], p[1], p[2], p[3], p[4], p[5], W, p[6], p[7],
+                                           B, Hkv, D, r, P, M, tpp, rows, cap, style, NUL)
+
+
+def test_fused_rejects_bad_arguments(lib):
+    assert _fused(lib, W=-1) == ERR["SHAPE"]
+    assert _fused(lib, rows=-1) == ERR["SHAPE"]
+    assert _fused(lib, cap=-1) == ERR["SHAPE"]
+    assert _fused(lib, W=1 << 20, B=1 << 12) == ERR["SHAPE"]  # 2^32 rows
+    assert _fused(lib, D=48, r=48) == ERR["HEAD_DIM"]
+    assert _fused(lib, r=200) == ERR["ROTARY_DIM"]
+    assert _fused(lib, style=3) == ERR["STYLE"]
+    assert _fused(lib, ptrs=[A, A, A, A, NUL, A, A, A, A]) == ERR["NULL"]
+    assert _fused(lib, ptrs=[A, A, A, A, A, A, MIS, A, A]) == ERR["MISALIGNED"]
+    assert _fused(lib, W=0) == OK and _fused(lib, B=0) == OK
+
+
+def test_metadata_and_gather_reject_bad_arguments(lib):
+    assert lib.dflash_prepare_delta_metadata(A, A, -1, A, A, 4, NUL) == ERR["SHAPE"]
+    assert lib.dflash_prepare_delta_metadata(A, A, 4, A, A, -4, NUL) == ERR["SHAPE"]
+    assert lib.dflash_prepare_delta_metadata(A, A, 4, NUL, A, 4, NUL) == ERR["NULL"]
+    assert lib.dflash_prepare_delta_metadata(A, A, 4, A, MIS, 4, NUL) == ERR["MISALIGNED"]
+    assert lib.dflash_prepare_delta_metadata(NUL, NUL, 0, NUL, NUL, 4, NUL) == OK
+    assert lib.dflash_gather_delta_rope(A, A, A, A, NUL, 8, 4, 1, 64, 72, NUL) == ERR["ROTARY_DIM"]
+    assert lib.dflash_gather_delta_rope(A, A, A, A, NUL, 8, 4, 1, 64, 512, NUL) == ERR["ROTARY_DIM"]
+    assert lib.dflash_gather_delta_rope(A, A, A, A, NUL, -8, 4, 1, 64, 64, NUL) == ERR["SHAPE"]
+    assert lib.dflash_gather_delta_rope(A, NUL, A, A, NUL, 8, 4, 1, 64, 64, NUL) == ERR["NULL"]
+    assert lib.dflash_gather_delta_rope(A, A, A, A, MIS, 8, 4, 1, 64, 64, NUL) == ERR["MISALIGNED"]
+    assert lib.dflash_gather_delta_rope(NUL, NUL, NUL, NUL, NUL, 0, 4, 1, 64, 64, NUL) == OK

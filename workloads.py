@@ -300,6 +300,105 @@ def make_paged(N, B, Hkv, D, r, tokens_per_page, max_pages_per_seq, num_pages, s
                      np.ascontiguousarray(table), name=name, extra={"lengths": L, "old": old})
 
 
+# ----------------------------------------------------- fused DFlash update --
+
+@dataclass
+class PagedFusedCase:
+    """Inputs of the one-launch DFlash update (metadata + gather + paged update):
+    rows laid out [B, W]; row b*W + j is sequence b's delta token j."""
+    B: int
+    W: int                    # deltaWidth
+    Hkv: int
+    D: int
+    r: int
+    num_pages: int
+    max_pages_per_seq: int
+    tokens_per_page: int
+    style: int
+    theta: float
+    k_delta: np.ndarray       # [B*W, Hkv, D] uint16
+    v_delta: np.ndarray       # [B*W, Hkv, D] uint16
+    source: np.ndarray        # [sourceRows, cacheCapacity, r] float32
+    old_lengths: np.ndarray   # [B] int32
+    delta_lengths: np.ndarray  # [B] int32
+    state: Optional[np.ndarray]  # [B] int32 or None
+    page_table: np.ndarray    # [B, 2, maxPagesPerSeq] int32
+    name: str = ""
+
+    @property
+    def N(self) -> int:
+        return self.B * self.W
+
+    def pool_shape(self):
+        return (2, self.num_pages, self.tokens_per_page, self.Hkv, self.D)
+
+    def new_pool(self) -> np.ndarray:
+        return sentinel_fill(self.pool_shape())
+
+    def plane_written(self):
+        """Boolean [B*W] masks of rows whose K / V plane is written (input
+        bookkeeping for byte counts: layout, page-table and capacity rules)."""
+        j = np.tile(np.arange(self.W), self.B)
+        b = np.repeat(np.arange(self.B), self.W)
+        pos = self.old_lengths[b].astype(np.int64) + j
+        ok = (j < self.delta_lengths[b]) & (pos >= 0)
+        lp = np.where(ok, pos // self.tokens_per_page, 0)
+        ok &= lp < self.max_pages_per_seq
+        lpc = np.where(ok, lp, 0)
+        idk = self.page_table[b, 0, lpc]
+        idv = self.page_table[b, 1, lpc]
+        kw = ok & (idk >= 0) & (idk < self.num_pages)
+        vw = ok & (idv >= self.num_pages) & (idv < 2 * self.num_pages)
+        return kw, vw
+
+    def algorithmic_bytes(self) -> int:
+        """8 B of lengths per sequence; per written K plane: K read + cos/sin row
+        + K written; per written V plane: V read + V written."""
+        kw, vw = self.plane_written()
+        row = self.Hkv * self.D * 2
+        return int(self.B * 8 + kw.sum() * (2 * row + self.r * 4) + vw.sum() * 2 * row)
+
+    @property
+    def valid_rows(self) -> int:
+        kw, vw = self.plane_written()
+        return int((kw | vw).sum())
+
+
+def make_paged_fused(B, W, Hkv, D, r, tokens_per_page, max_pages_per_seq, num_pages, style, theta,
+                     seed, len_range=None, unmapped_frac=0.02, source_rows=1, with_state=False,
+                     cache_capacity=None, name="paged_fused") -> PagedFusedCase:
+    """Delta lengths uniform in len_range (default 1..W), old lengths uniform so
+    that every token fits the sequence's logical pages, page ids as make_paged,
+    a cos/sin source of `source_rows` tables (row k shifted by k*1000 positions)
+    of cache_capacity positions, optional per-sequence state indices."""
+    rng = rng_for(seed)
+    k_delta = fp16_normal(rng, (B * W, Hkv, D))
+    v_delta = fp16_normal(rng, (B * W, Hkv, D))
+    lo, hi = len_range if len_range is not None else (1, W)
+    lengths = rng.integers(lo, hi + 1, size=B).astype(np.int32)
+    max_position = max_pages_per_seq * tokens_per_page
+    old = np.array([rng.integers(0, max(1, max_position - max(int(l), 0) + 1)) for l in lengths],
+                   dtype=np.int32)
+    n_logical = B * max_pages_per_seq
+    reps = -(-n_logical // num_pages)
+    kperm = np.concatenate([rng.permutation(num_pages) for _ in range(reps)])[:n_logical]
+    vperm = np.concatenate([rng.permutation(num_pages) for _ in range(reps)])[:n_logical]
+    table = np.empty((B, 2, max_pages_per_seq), dtype=np.int32)
+    table[:, 0, :] = kperm.reshape(B, max_pages_per_seq)
+    table[:, 1, :] = (vperm + num_pages).reshape(B, max_pages_per_seq)
+    n_unmapped = int(round(unmapped_frac * table.size))
+    if n_unmapped:
+        flat = table.reshape(-1)
+        flat[rng.choice(table.size, size=n_unmapped, replace=False)] = -1
+    cap = max_position if cache_capacity is None else cache_capacity
+    offs = np.arange(source_rows) * 1000
+    source = cos_sin_table(theta, cap, r, batch=source_rows, pos_offset=offs)
+    state = rng.integers(0, source_rows, size=B).astype(np.int32) if with_state else None
+    return PagedFusedCase(B, W, Hkv, D, r, num_pages, max_pages_per_seq, tokens_per_page, style,
+                          theta, k_delta, v_delta, source, old, lengths, state,
+                          np.ascontiguousarray(table), name=name)
+
+
 # ------------------------------------------------------------ the configs --
 
 CONFIG_NAMES = ("packed_tiny", "prefill", "decode", "tree", "paged")
@@ -308,6 +407,9 @@ CONFIG_NAMES = ("packed_tiny", "prefill", "decode", "tree", "paged")
 # tokens / rows per launch, a smaller cache (decode: capacity 1024) or pool
 # (paged: 64 logical pages per sequence, 8192 pages per plane, positions < 4096).
 PROFILE_NAMES = ("decode_c1024", "paged_p8192")
+
+# Workloads of the next rows (built on the same kernels).
+NEXT_NAMES = ("paged_fused",)
 
 
 def config(name: str):
@@ -345,6 +447,13 @@ def config(name: str):
     if name == "paged_p8192":
         return make_paged(16384, 128, 8, 128, 128, 64, 64, 8192, NEOX, 5e5, seed=4,
                           valid_rows=15565, name=name)
+    if name == "paged_fused":
+        # the DFlash step in one launch: B=128 sequences x deltaWidth 128 rows
+        # (16384 rows), delta lengths uniform in [1, 128], Hkv=8, D=r=128,
+        # 64 tokens/page, 512 pages/seq, 65536 pages per plane, one shared
+        # cos/sin table of 32768 positions.
+        return make_paged_fused(128, 128, 8, 128, 128, 64, 512, 65536, NEOX, 5e5, seed=5,
+                                name=name)
     if name == "paged":
         # 16384 delta rows over 128 sequences (15565 valid), Hkv=8, D=r=128,
         # 64 tokens/page, 512 logical pages per sequence, 65536 pages per plane.
@@ -362,13 +471,30 @@ def step_variant(case, k: int):
     Contiguous cases: (end_lens, pos_ids) -- new per-sequence start/end offsets
     (and tree bases) so every step writes different cache slots. Paged cases:
     page_table -- fresh page permutations with the same unmapped fraction, so
-    every step writes different pages.
+    every step writes different pages. Fused DFlash cases: (old_lengths,
+    page_table).
     """
     if k == 0:
         if isinstance(case, PagedCase):
             return case.page_table
+        if isinstance(case, PagedFusedCase):
+            return case.old_lengths, case.page_table
         return case.end_lens, case.pos_ids
     rng = rng_for(1000 + k)
+    if isinstance(case, PagedFusedCase):
+        max_position = case.max_pages_per_seq * case.tokens_per_page
+        old = np.array([rng.integers(0, max(1, max_position - max(int(l), 0) + 1))
+                        for l in case.delta_lengths], dtype=np.int32)
+        t = case.page_table.copy()
+        B, _, M = t.shape
+        n = B * M
+        reps = -(-n // case.num_pages)
+        kp = np.concatenate([rng.permutation(case.num_pages) for _ in range(reps)])[:n]
+        vp = np.concatenate([rng.permutation(case.num_pages) for _ in range(reps)])[:n]
+        t[:, 0, :] = kp.reshape(B, M)
+        t[:, 1, :] = (vp + case.num_pages).reshape(B, M)
+        t[case.page_table < 0] = -1
+        return old, np.ascontiguousarray(t)
     if isinstance(case, PagedCase):
         t = case.page_table.copy()
         B, _, M = t.shape
