@@ -40,7 +40,8 @@ import workloads  # noqa: E402
 
 METRIC = "fused RoPE+KV-write tokens/s and effective HBM GB/s (% of GB300 peak)"
 HEADLINE = "prefill"
-EXTRA = ("decode", "tree", "paged", "packed_tiny", "paged_fused", "paged_fused_3launch")
+EXTRA = ("decode", "tree", "paged", "packed_tiny", "paged_fused", "paged_fused_3launch",
+         "slotmap_prefill", "slotmap_decode")
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 
@@ -58,6 +59,10 @@ DESCR = {
                    "B=128 x deltaWidth 128 rows, lengths in [1,128], Hkv=8 D=r=128 NeoX, "
                    "64 tokens/page, 512 pages/seq, 65536 pages per plane",
     "paged_fused_3launch": "the same DFlash step as three launches (metadata, gather, update)",
+    "slotmap_prefill": "the prefill behind the sglang-style interface: separate Q/K/V views of a "
+                       "packed buffer, per-token positions and flat slots, block size 64, "
+                       "16384 blocks",
+    "slotmap_decode": "256 one-token decodes behind the sglang-style interface",
     "decode_c1024": "decode as above with cache capacity 1024 (profiler-sized twin)",
     "paged_p8192": "paged as above with 64 pages/seq and 8192 pages per plane (profiler-sized twin)",
 }
@@ -187,6 +192,7 @@ class DeviceWorkload:
         self.case = workloads.config(name[: -len("_3launch")] if self.three_launch else name)
         self.paged = isinstance(self.case, workloads.PagedCase)
         self.fused = isinstance(self.case, workloads.PagedFusedCase)
+        self.slotmap = isinstance(self.case, workloads.SlotMapCase)
         c = self.case
         if self.paged or self.fused:
             self.tokens = c.valid_rows
@@ -223,6 +229,15 @@ class DeviceWorkload:
                     st["cs"] = torch.empty((c.N, c.r), dtype=torch.float32, device=device)
                 self.sets.append(st)
             self.bytes = int(np.mean([self._variant_bytes(k) for k in range(self.ring)]))
+        elif self.slotmap:
+            self.cos_sin = t(c.cos_sin)
+            self.kc = self._sentinel(c.cache_shape())
+            self.vc = self._sentinel(c.cache_shape())
+            qkv_base = t(c.qkv)
+            for k in range(self.ring):
+                pos, slots = workloads.step_variant(c, k)
+                self.sets.append(dict(qkv=qkv_base.clone() if k else qkv_base, pos=t(pos),
+                                      slots=t(slots), qout=self._sentinel((c.T, c.Hq, c.D))))
         else:
             self.cos_sin = t(c.cos_sin)
             self.cache = (t(c.new_cache()) if c.cache_init == "zero"
@@ -277,6 +292,12 @@ class DeviceWorkload:
                                         batch_size=c.B, stream=stream)
             rk.paged_kv_delta_update(s["k"], s["v"], self.pool, s["cs"], s["pos"], s["seq"],
                                      s["pt"], style=c.style, stream=stream)
+        elif self.slotmap:
+            qkv = s["qkv"]
+            Hq, Hkv = c.Hq, c.Hkv
+            rk.rope_write_kv_slot_mapping(self.cos_sin, s["pos"], qkv[:, :Hq], qkv[:, Hq:Hq + Hkv],
+                                          qkv[:, Hq + Hkv:], s["slots"], self.kc, self.vc,
+                                          s["qout"], None, style=c.style, stream=stream)
         elif self.fused:
             rk.paged_kv_delta_update_fused(s["k"], s["v"], self.pool, self.source, s["old"],
                                            self.lens, s["pt"], self.state, style=c.style,
@@ -558,7 +579,8 @@ def main(argv=None):
     launch_s = sec / args.steps
     achieved = wl.bytes / launch_s / 1e9
     clocks = sampler.summary(t0, t1) if sampler else None
-    e2e = e2e_contiguous(wl, args.e2e_steps) if not (wl.paged or wl.fused) else None
+    e2e = e2e_contiguous(wl, args.e2e_steps) \
+        if not (wl.paged or wl.fused or wl.slotmap) else None
     tokens, bytes_step, ring = wl.tokens, wl.bytes, wl.ring
     kernel = _kernel_name(wl)
     del wl
@@ -632,6 +654,8 @@ def main(argv=None):
 
 def _kernel_name(wl) -> str:
     c = wl.case
+    if wl.slotmap:
+        return f"rope_kv_slotmap_kernel<D={c.D}, {'NeoX' if c.style == 0 else 'GPT-J'}>"
     if wl.fused:
         if wl.three_launch:
             return "delta_metadata_kernel + gather_delta_rope_kernel + paged_delta_kernel"

@@ -14,7 +14,8 @@
  *         (launchDFlashTargetKVCacheUpdate, checkDFlashRopeCapacity,
  *         launchDFlashPrepareDeltaMetadata, launchDFlashGatherDeltaRope).
  *   [RC]  sglang rope_cache.py (_get_neox_rotated_x, _get_gptj_rotated_x,
- *         _unit_rope, _load_cos_sin, kernel Stage 2.1).
+ *         _unit_rope, _load_cos_sin, kernel Stage 2.1; the
+ *         fused_qk_rope_reshape_and_cache interface, Stages 3.1-3.5).
  *
  * Common rules for every entry point:
  *   - FP16 tensors are uint16_t arrays holding IEEE binary16 bits; FP32 tables
@@ -164,6 +165,39 @@ ROPEKV_API int paged_kv_delta_update(const uint16_t* kDelta, const uint16_t* vDe
                                      int32_t rotaryDim, int32_t numPages,
                                      int32_t maxPagesPerSeq, int32_t tokensPerPage,
                                      int32_t style, void* stream);
+
+/*
+ * [RC] fused_qk_rope_reshape_and_cache with the flash cache layout: the same
+ * fused RoPE + KV write behind sglang's interface. Q, K and V are separate
+ * token-major tensors that may be views into one packed QKV buffer; every token
+ * carries its own RoPE position and one flat cache slot.
+ *   cosSin       [cosSinRows, rotaryDim] FP32, row = position.
+ *   positions    [numTokens] INT64 RoPE position of each token.
+ *   q            [numTokens, numQHeads, headDim] FP16, token stride qTokenStride
+ *                elements (>= numQHeads*headDim, a multiple of 8); k, v likewise
+ *                with numKVHeads heads and their own strides. Read only.
+ *   slotMapping  [numTokens] INT64 flat slot: block slot / blockSize, offset
+ *                slot % blockSize.
+ *   keyCache, valueCache  [numBlocks, blockSize, numKVHeads, headDim] FP16, written
+ *                at the slots (rotated K; V bits).
+ *   qOut         [numTokens, numQHeads, headDim] FP16, rotated Q, written.
+ *   kOut         [numTokens, numKVHeads, headDim] FP16 rotated K, or NULL.
+ * A negative slot, or one >= numBlocks*blockSize, skips the cache writes and
+ * kOut for that token (its qOut row is still written). A position outside
+ * [0, cosSinRows) skips the whole token.
+ * Host errors: strides too small or not multiples of 8 -> ROPEKV_ERR_SHAPE.
+ */
+ROPEKV_API int rope_write_kv_slot_mapping(const float* cosSin, const int64_t* positions,
+                                          const uint16_t* q, int64_t qTokenStride,
+                                          const uint16_t* k, int64_t kTokenStride,
+                                          const uint16_t* v, int64_t vTokenStride,
+                                          const int64_t* slotMapping, uint16_t* keyCache,
+                                          uint16_t* valueCache, uint16_t* qOut, uint16_t* kOut,
+                                          int32_t numTokens, int32_t numQHeads,
+                                          int32_t numKVHeads, int32_t headDim,
+                                          int32_t rotaryDim, int32_t cosSinRows,
+                                          int64_t numBlocks, int32_t blockSize, int32_t style,
+                                          void* stream);
 
 /*
  * The DFlash target-KV step as ONE launch: launchDFlashPrepareDeltaMetadata,

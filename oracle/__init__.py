@@ -96,6 +96,10 @@ def _load():
     lib.ropekv_oracle_gather_delta_rope.restype = I
     lib.ropekv_oracle_paged_fused.argtypes = [P] * 9 + [I] * 10
     lib.ropekv_oracle_paged_fused.restype = I
+    L = ctypes.c_int64
+    lib.ropekv_oracle_slot_mapping.argtypes = [P, P, P, L, P, L, P, L, P, P, P, P, P,
+                                               I, I, I, I, I, I, L, I, I]
+    lib.ropekv_oracle_slot_mapping.restype = I
     lib.ropekv_oracle_capacity_rejected.argtypes = [ctypes.c_int32, ctypes.c_int32]
     lib.ropekv_oracle_capacity_rejected.restype = I
     _lib = lib
@@ -289,6 +293,32 @@ def paged_fused(k_delta, v_delta, kv_pool, source, old_lengths, delta_lengths, d
         _ptr(np.ascontiguousarray(delta_lengths, dtype=np.int32), np.int32), delta_width, st,
         _ptr(page_table, np.int32), B, Hkv, D, r, num_pages, mpps, tpp, rows, cap, style)
     _check(rc, "paged_fused")
+
+
+def slot_mapping(cos_sin, positions, q, k, v, slots, key_cache, value_cache, q_out, k_out,
+                 style):
+    """sglang-style call on host arrays. q [T, Hq, D], k / v [T, Hkv, D] may be
+    token-strided views (their last two dims contiguous); caches [blocks,
+    blockSize, Hkv, D]; q_out [T, Hq, D]; k_out [T, Hkv, D] or None. Mutates the
+    caches, q_out and k_out."""
+    rows, r = cos_sin.shape
+    T, Hq, D = q.shape
+    Hkv = k.shape[1]
+    blocks, bsz = key_cache.shape[:2]
+
+    def strided(a):
+        assert a.dtype == np.uint16 and a.strides[2] == 2 and a.strides[1] == a.shape[2] * 2
+        return ctypes.c_void_p(a.ctypes.data), a.strides[0] // 2
+
+    qp, qs = strided(q)
+    kp, ks = strided(k)
+    vp, vs = strided(v)
+    kop = ctypes.c_void_p(0) if k_out is None else _ptr(k_out, np.uint16)
+    rc = _load().ropekv_oracle_slot_mapping(
+        _ptr(cos_sin, np.float32), _ptr(positions, np.int64), qp, qs, kp, ks, vp, vs,
+        _ptr(slots, np.int64), _ptr(key_cache, np.uint16), _ptr(value_cache, np.uint16),
+        _ptr(q_out, np.uint16), kop, T, Hq, Hkv, D, r, rows, blocks, bsz, style)
+    _check(rc, "slot_mapping")
 
 
 def capacity_rejected(cos_sin_seq_len: int, kv_capacity: int) -> bool:

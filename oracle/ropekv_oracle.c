@@ -422,6 +422,44 @@ int ropekv_oracle_paged_fused(const uint16_t* kDelta, const uint16_t* vDelta, ui
     return rc;
 }
 
+int ropekv_oracle_slot_mapping(const float* cosSin, const int64_t* positions,
+                               const uint16_t* q, int64_t qStride, const uint16_t* k,
+                               int64_t kStride, const uint16_t* v, int64_t vStride,
+                               const int64_t* slotMapping, uint16_t* keyCache,
+                               uint16_t* valueCache, uint16_t* qOut, uint16_t* kOut, int T,
+                               int Hq, int Hkv, int D, int r, int cosSinRows, int64_t numBlocks,
+                               int blockSize, int style)
+{
+    if (T < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || D <= 0 || r <= 0 || r % 2 != 0 ||
+        r > D || cosSinRows < 0 || numBlocks < 0 || blockSize <= 0 ||
+        (style != STYLE_NEOX && style != STYLE_GPTJ))
+        return -1;
+    int64_t slots = numBlocks * (int64_t)blockSize;
+    for (int t = 0; t < T; ++t) {
+        int64_t pos = positions[t];
+        if (pos < 0 || pos >= cosSinRows)
+            continue; /* no table row: nothing is written for the token */
+        const float* cs = cosSin + (size_t)pos * r;
+        for (int hq = 0; hq < Hq; ++hq)
+            rope_head_f16(q + (size_t)t * qStride + (size_t)hq * D, cs, D, r, style,
+                          qOut + ((size_t)t * Hq + hq) * D);
+        int64_t slot = slotMapping[t];
+        if (slot < 0 || slot >= slots)
+            continue; /* the cache write (and kOut) is skipped */
+        int64_t block = slot / blockSize;
+        int64_t off = slot % blockSize;
+        for (int hk = 0; hk < Hkv; ++hk) {
+            uint16_t* kc = keyCache + (((size_t)block * blockSize + off) * Hkv + hk) * D;
+            rope_head_f16(k + (size_t)t * kStride + (size_t)hk * D, cs, D, r, style, kc);
+            if (kOut != NULL)
+                memcpy(kOut + ((size_t)t * Hkv + hk) * D, kc, sizeof(uint16_t) * (size_t)D);
+            uint16_t* vc = valueCache + (((size_t)block * blockSize + off) * Hkv + hk) * D;
+            memcpy(vc, v + (size_t)t * vStride + (size_t)hk * D, sizeof(uint16_t) * (size_t)D);
+        }
+    }
+    return 0;
+}
+
 int ropekv_oracle_capacity_rejected(int32_t cosSinSeqLen, int32_t kvCapacity)
 {
     /* the RoPE table may be shorter than the page-aligned capacity; only a

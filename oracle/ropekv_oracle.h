@@ -14,6 +14,8 @@
  *   [RC]  sglang python/sglang/kernels/ops/kvcache/rope_cache.py:
  *         _get_neox_rotated_x, _get_gptj_rotated_x, _unit_rope, _load_cos_sin,
  *         kernel Stage 2.1 (frequency index) and the wrapper's cos_sin width rule.
+ *   [RC]  (also) fused_qk_rope_reshape_and_cache, flash layout: separate Q/K/V,
+ *         a flat slot mapping, the KV write skipped for negative slots.
  *   [DRK] TensorRT-Edge-LLM C++ API, "Dflash Runtime Kernels":
  *         launchDFlashTargetKVCacheUpdate, checkDFlashRopeCapacity,
  *         launchDFlashPrepareDeltaMetadata, launchDFlashGatherDeltaRope,
@@ -147,6 +149,23 @@ int ropekv_oracle_paged_fused(const uint16_t* kDelta, const uint16_t* vDelta, ui
                               int batchSize, int Hkv, int D, int r, int numPages,
                               int maxPagesPerSeq, int tokensPerPage, int sourceRows,
                               int cacheCapacity, int style);
+
+/* [RC] fused_qk_rope_reshape_and_cache with the flash cache layout.
+ * Token t (of T) has RoPE position positions[t] (row of cosSin [cosSinRows, r])
+ * and flat cache slot slotMapping[t]. Q [T, Hq, D], K and V [T, Hkv, D] are read
+ * with token strides qStride / kStride / vStride (elements). Rotated Q goes to
+ * qOut [T, Hq, D]. When 0 <= slot < numBlocks*blockSize, rotated K goes to
+ * keyCache[slot / blockSize, slot % blockSize] and to kOut [T, Hkv, D] (kOut
+ * may be NULL), and V's bits go to valueCache at the same place; both caches
+ * are [numBlocks, blockSize, Hkv, D]. A negative slot (or one past the caches)
+ * skips those writes only. A position outside [0, cosSinRows) skips the token. */
+int ropekv_oracle_slot_mapping(const float* cosSin, const int64_t* positions,
+                               const uint16_t* q, int64_t qStride, const uint16_t* k,
+                               int64_t kStride, const uint16_t* v, int64_t vStride,
+                               const int64_t* slotMapping, uint16_t* keyCache,
+                               uint16_t* valueCache, uint16_t* qOut, uint16_t* kOut, int T,
+                               int Hq, int Hkv, int D, int r, int cosSinRows, int64_t numBlocks,
+                               int blockSize, int style);
 
 /* [DRK] checkDFlashRopeCapacity: 1 when the pair is rejected
  * (cosSinSeqLen > kvCapacity), else 0. */

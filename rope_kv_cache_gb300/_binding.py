@@ -63,12 +63,16 @@ def load_library():
     lib.paged_kv_delta_update_fused.argtypes = [P] * 6 + [I32] + [P] * 2 + [I32] * 10 + [P]
     lib.dflash_prepare_delta_metadata.argtypes = [P, P, I32, P, P, I32, P]
     lib.dflash_gather_delta_rope.argtypes = [P] * 5 + [I32] * 5 + [P]
+    I64 = ctypes.c_int64
+    lib.rope_write_kv_slot_mapping.argtypes = [P, P, P, I64, P, I64, P, I64, P, P, P, P, P,
+                                               I32, I32, I32, I32, I32, I32, I64, I32, I32, P]
     lib.rope_check_capacity.argtypes = [I32, I32]
     lib.ropekv_status_string.argtypes = [ctypes.c_int]
     lib.ropekv_status_string.restype = ctypes.c_char_p
     for fn in ("rope_write_kv_packed", "rope_write_kv_continuous", "rope_write_kv_tree",
                "paged_kv_delta_update", "paged_kv_delta_update_fused",
-               "dflash_prepare_delta_metadata", "dflash_gather_delta_rope", "rope_check_capacity"):
+               "dflash_prepare_delta_metadata", "dflash_gather_delta_rope",
+               "rope_write_kv_slot_mapping", "rope_check_capacity"):
         getattr(lib, fn).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -103,7 +107,22 @@ def _dev_ptr(t: Optional[torch.Tensor], name: str, dtypes, device) -> ctypes.c_v
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _dev_rows(t: torch.Tensor, name: str, device):
+    """Pointer and token stride of a [T, H, D] FP16 tensor whose last two dims
+    are dense (a token-strided view, e.g. a slice of a packed QKV buffer)."""
+    if not isinstance(t, torch.Tensor) or t.dim() != 3:
+        raise ValueError(f"{name} must be a [T, H, D] tensor")
+    if t.dtype not in _F16:
+        raise TypeError(f"{name}: dtype {t.dtype} not in {_F16}")
+    if t.device.type != "cuda" or t.device != device:
+        raise ValueError(f"{name} must be on {device}")
+    if t.stride(2) != 1 or t.stride(1) != t.shape[2]:
+        raise ValueError(f"{name}: heads and dims must be dense (strides (*, D, 1))")
+    return ctypes.c_void_p(t.data_ptr()), int(t.stride(0))
+
+
 _F16 = (torch.float16, torch.int16)
+_I64 = (torch.int64,)
 _F32 = (torch.float32,)
 _I32 = (torch.int32,)
 
@@ -313,3 +332,36 @@ def dflash_gather_delta_rope(source: torch.Tensor, output: torch.Tensor,
         _dev_ptr(state_indices, "state_indices", _I32, dev), N, int(batch_size), rows, cap, r,
         _stream_handle(stream, dev))
     _check_rc("dflash_gather_delta_rope", rc)
+
+
+def rope_write_kv_slot_mapping(cos_sin: torch.Tensor, positions: torch.Tensor, q: torch.Tensor,
+                               k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
+                               key_cache: torch.Tensor, value_cache: torch.Tensor,
+                               q_out: torch.Tensor, k_out: Optional[torch.Tensor] = None,
+                               style: int = NEOX,
+                               stream: Optional[torch.cuda.Stream] = None) -> None:
+    """sglang-style interface: cos_sin [rows, r] float32; positions, slot_mapping
+    [T] int64; q [T, Hq, D], k, v [T, Hkv, D] float16 (token-strided views allowed);
+    key_cache, value_cache [blocks, block_size, Hkv, D] float16; q_out [T, Hq, D];
+    k_out [T, Hkv, D] or None. A negative slot skips that token's cache writes."""
+    dev = q.device
+    T, Hq, D = q.shape
+    Hkv = k.shape[1]
+    if cos_sin.dim() != 2 or tuple(k.shape) != (T, Hkv, D) or tuple(v.shape) != (T, Hkv, D) \
+            or tuple(positions.shape) != (T,) or tuple(slot_mapping.shape) != (T,) \
+            or key_cache.dim() != 4 or tuple(key_cache.shape[2:]) != (Hkv, D) \
+            or tuple(value_cache.shape) != tuple(key_cache.shape) \
+            or tuple(q_out.shape) != (T, Hq, D) \
+            or (k_out is not None and tuple(k_out.shape) != (T, Hkv, D)):
+        raise ValueError("inconsistent shapes for rope_write_kv_slot_mapping")
+    qp, qs = _dev_rows(q, "q", dev)
+    kp, ks = _dev_rows(k, "k", dev)
+    vp, vs = _dev_rows(v, "v", dev)
+    rc = load_library().rope_write_kv_slot_mapping(
+        _dev_ptr(cos_sin, "cos_sin", _F32, dev), _dev_ptr(positions, "positions", _I64, dev),
+        qp, qs, kp, ks, vp, vs, _dev_ptr(slot_mapping, "slot_mapping", _I64, dev),
+        _dev_ptr(key_cache, "key_cache", _F16, dev), _dev_ptr(value_cache, "value_cache", _F16, dev),
+        _dev_ptr(q_out, "q_out", _F16, dev), _dev_ptr(k_out, "k_out", _F16, dev),
+        T, Hq, Hkv, D, cos_sin.shape[1], cos_sin.shape[0], key_cache.shape[0], key_cache.shape[1],
+        style, _stream_handle(stream, dev))
+    _check_rc("rope_write_kv_slot_mapping", rc)

@@ -445,6 +445,95 @@ int dflash_gather_delta_rope(const float* source, float* output, const int32_t* 
     return launch_status();
 }
 
+int rope_write_kv_slot_mapping(const float* cosSin, const int64_t* positions, const uint16_t* q,
+                               int64_t qTokenStride, const uint16_t* k, int64_t kTokenStride,
+                               const uint16_t* v, int64_t vTokenStride,
+                               const int64_t* slotMapping, uint16_t* keyCache,
+                               uint16_t* valueCache, uint16_t* qOut, uint16_t* kOut,
+                               int32_t numTokens, int32_t numQHeads, int32_t numKVHeads,
+                               int32_t headDim, int32_t rotaryDim, int32_t cosSinRows,
+                               int64_t numBlocks, int32_t blockSize, int32_t style, void* stream)
+{
+    if (style != ROPEKV_NEOX && style != ROPEKV_GPTJ)
+        return ROPEKV_ERR_STYLE;
+    int rc = check_head_dims(headDim, rotaryDim);
+    if (rc != ROPEKV_OK)
+        return rc;
+    if (numQHeads <= 0 || numKVHeads <= 0 || numQHeads % numKVHeads != 0)
+        return ROPEKV_ERR_HEADS;
+    if (numTokens < 0 || cosSinRows < 0 || numBlocks < 0 || blockSize <= 0 ||
+        numBlocks > (1LL << 40))
+        return ROPEKV_ERR_SHAPE;
+    if (qTokenStride < (int64_t)numQHeads * headDim || kTokenStride < (int64_t)numKVHeads * headDim ||
+        vTokenStride < (int64_t)numKVHeads * headDim || (qTokenStride % 8) != 0 ||
+        (kTokenStride % 8) != 0 || (vTokenStride % 8) != 0)
+        return ROPEKV_ERR_SHAPE;
+    const long long items = ((long long)numQHeads + 2LL * numKVHeads) * (headDim / 16);
+    if (items > (1LL << 30))
+        return ROPEKV_ERR_SHAPE;
+    if (numTokens == 0)
+        return ROPEKV_OK;
+    if (!cosSin || !positions || !q || !k || !v || !slotMapping || !keyCache || !valueCache ||
+        !qOut)
+        return ROPEKV_ERR_NULL_POINTER;
+    if (!aligned16(cosSin) || !aligned16(positions) || !aligned16(q) || !aligned16(k) ||
+        !aligned16(v) || !aligned16(slotMapping) || !aligned16(keyCache) ||
+        !aligned16(valueCache) || !aligned16(qOut) || !aligned16(kOut))
+        return ROPEKV_ERR_MISALIGNED;
+    ropekv::SlotMapArgs a = {};
+    a.cosSin = cosSin;
+    a.positions = positions;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.slots = slotMapping;
+    a.keyCache = keyCache;
+    a.valueCache = valueCache;
+    a.qOut = qOut;
+    a.kOut = kOut;
+    a.qStride = qTokenStride;
+    a.kStride = kTokenStride;
+    a.vStride = vTokenStride;
+    a.numSlots = numBlocks * (int64_t)blockSize;
+    a.Hq = numQHeads;
+    a.Hkv = numKVHeads;
+    a.r = rotaryDim;
+    a.csRows = cosSinRows;
+    a.itemsPerToken = (int32_t)items;
+    const Shape sh = pick_shape(a.itemsPerToken, numTokens);
+    if ((long long)numTokens * sh.ctasPerUnit > 0x7FFFFFFFLL)
+        return ROPEKV_ERR_SHAPE;
+    a.ctasPerToken = sh.ctasPerUnit;
+    const unsigned grid = (unsigned)((long long)numTokens * sh.ctasPerUnit);
+    cudaStream_t st = (cudaStream_t)stream;
+    const bool gptj = style == ROPEKV_GPTJ;
+#define ROPEKV_SLOTMAP_LAUNCH(DD)                                                            \
+    do {                                                                                   \
+        if (sh.ipt == 2) {                                                                 \
+            if (gptj)                                                                      \
+                ropekv::rope_kv_slotmap_kernel<DD, ropekv::kGptj, 2, kPolicy>              \
+                    <<<grid, sh.threads, 0, st>>>(a);                                      \
+            else                                                                           \
+                ropekv::rope_kv_slotmap_kernel<DD, ropekv::kNeox, 2, kPolicy>              \
+                    <<<grid, sh.threads, 0, st>>>(a);                                      \
+        } else {                                                                           \
+            if (gptj)                                                                      \
+                ropekv::rope_kv_slotmap_kernel<DD, ropekv::kGptj, 1, kPolicy>              \
+                    <<<grid, sh.threads, 0, st>>>(a);                                      \
+            else                                                                           \
+                ropekv::rope_kv_slotmap_kernel<DD, ropekv::kNeox, 1, kPolicy>              \
+                    <<<grid, sh.threads, 0, st>>>(a);                                      \
+        }                                                                                  \
+    } while (0)
+    switch (headDim) {
+    case 64: ROPEKV_SLOTMAP_LAUNCH(64); break;
+    case 128: ROPEKV_SLOTMAP_LAUNCH(128); break;
+    default: ROPEKV_SLOTMAP_LAUNCH(256); break;
+    }
+#undef ROPEKV_SLOTMAP_LAUNCH
+    return launch_status();
+}
+
 int rope_check_capacity(int32_t cosSinSeqLen, int32_t kvCapacity)
 {
     return cosSinSeqLen > kvCapacity ? ROPEKV_ERR_CAPACITY : ROPEKV_OK;

@@ -69,6 +69,24 @@ struct PagedArgs {
     int32_t ctasPerRow;
 };
 
+// Arguments of the flat slot-mapping kernel (sglang-style separate Q/K/V).
+struct SlotMapArgs {
+    const float* cosSin;       // [csRows, r]
+    const int64_t* positions;  // [T]
+    const uint16_t* q;         // [T, Hq, D] with token stride qStride (elements)
+    const uint16_t* k;         // [T, Hkv, D] with token stride kStride
+    const uint16_t* v;         // [T, Hkv, D] with token stride vStride
+    const int64_t* slots;      // [T] flat cache slots
+    uint16_t* keyCache;        // [numBlocks, blockSize, Hkv, D]
+    uint16_t* valueCache;      // [numBlocks, blockSize, Hkv, D]
+    uint16_t* qOut;            // [T, Hq, D]
+    uint16_t* kOut;            // [T, Hkv, D] or NULL
+    int64_t qStride, kStride, vStride, numSlots;
+    int32_t Hq, Hkv, r, csRows;
+    int32_t itemsPerToken;     // (Hq + 2 Hkv) * D / 16
+    int32_t ctasPerToken;
+};
+
 // Arguments of the DFlash delta-metadata and cos/sin gather kernels.
 struct DeltaMetaArgs {
     const int32_t* oldLens;    // [B]
@@ -474,6 +492,96 @@ __global__ void __launch_bounds__(256) paged_delta_kernel(const PagedArgs a)
         uint16_t* dst = a.pool + ((size_t)id * a.tpp + inPage) * rowElems + (size_t)head * D;
         store_v<POL>(dst + 8 * va, xa[k], pol);
         store_v<POL>(dst + 8 * vb, xb[k], pol);
+    }
+}
+
+// ------------------------------------------------- slot-mapping kernel --
+//
+// sglang rope_cache.py, fused_qk_rope_reshape_and_cache (flash layout): Q, K, V
+// come as separate token-strided tensors, each token carries its own RoPE
+// position and one flat cache slot (block = slot / blockSize, offset =
+// slot % blockSize, which for the [blocks, blockSize, Hkv, D] layout is simply
+// row `slot`). Rotated Q always goes to qOut; a negative slot (or one past the
+// caches) skips the K/V cache writes and kOut (Stage 3.1-3.5). Same item
+// decomposition as rope_kv_token_kernel; every K/V vector has one writer, so no
+// GQA group leader is needed.
+template <int D, int STYLE, int IPT, int POL>
+__global__ void __launch_bounds__(256) rope_kv_slotmap_kernel(const SlotMapArgs a)
+{
+    constexpr int kItemsPerHead = D / 16;
+    grid_dependency_sync<POL>();
+    const L2Policies pol = make_policies<POL>();
+    const int tok = blockIdx.x / a.ctasPerToken;
+    const int part = blockIdx.x - tok * a.ctasPerToken;
+    const int i = threadIdx.x % kItemsPerHead;
+    const int item0 = part * blockDim.x * IPT + threadIdx.x;
+    const int qkHeads = a.Hq + a.Hkv;
+
+    int va, vb;
+    item_vectors<D>(i, a.r, va, vb);
+
+    uint4 xa[IPT], xb[IPT];
+#pragma unroll
+    for (int k = 0; k < IPT; ++k) {
+        const int item = item0 + k * blockDim.x;
+        if (item < a.itemsPerToken) {
+            const int head = item / kItemsPerHead;
+            const uint16_t* p;
+            if (head < a.Hq)
+                p = a.q + tok * a.qStride + (size_t)head * D;
+            else if (head < qkHeads)
+                p = a.k + tok * a.kStride + (size_t)(head - a.Hq) * D;
+            else
+                p = a.v + tok * a.vStride + (size_t)(head - qkHeads) * D;
+            xa[k] = load_ro<POL>(p + 8 * va, pol);
+            xb[k] = load_ro<POL>(p + 8 * vb, pol);
+        }
+    }
+
+    const int64_t pos = __ldg(a.positions + tok);
+    if (pos < 0 || pos >= a.csRows)
+        return;  // no cos/sin row: nothing written for the token
+    const int64_t slot = __ldg(a.slots + tok);
+    const bool kvOk = slot >= 0 && slot < a.numSlots;
+
+    float c[8], sn[8];
+    const bool rotItem = i < (a.r >> 4);
+    if (rotItem)
+        load_cos_sin<STYLE, POL>(a.cosSin + pos * a.r, i, a.r, c, sn, pol);
+
+#pragma unroll
+    for (int k = 0; k < IPT; ++k) {
+        const int item = item0 + k * blockDim.x;
+        if (item >= a.itemsPerToken)
+            continue;
+        const int head = item / kItemsPerHead;
+        if (head < a.Hq) {
+            if (rotItem)
+                rotate_item<STYLE>(xa[k], xb[k], c, sn);
+            uint16_t* dst = a.qOut + ((size_t)tok * a.Hq + head) * D;
+            store_v<POL>(dst + 8 * va, xa[k], pol);
+            store_v<POL>(dst + 8 * vb, xb[k], pol);
+            continue;
+        }
+        if (!kvOk)
+            continue;
+        if (head < qkHeads) {
+            const int hk = head - a.Hq;
+            if (rotItem)
+                rotate_item<STYLE>(xa[k], xb[k], c, sn);
+            uint16_t* dst = a.keyCache + ((size_t)slot * a.Hkv + hk) * D;
+            store_v<POL>(dst + 8 * va, xa[k], pol);
+            store_v<POL>(dst + 8 * vb, xb[k], pol);
+            if (a.kOut != nullptr) {
+                uint16_t* ko = a.kOut + ((size_t)tok * a.Hkv + hk) * D;
+                store_v<POL>(ko + 8 * va, xa[k], pol);
+                store_v<POL>(ko + 8 * vb, xb[k], pol);
+            }
+        } else {
+            uint16_t* dst = a.valueCache + ((size_t)slot * a.Hkv + (head - qkHeads)) * D;
+            store_v<POL>(dst + 8 * va, xa[k], pol);
+            store_v<POL>(dst + 8 * vb, xb[k], pol);
+        }
     }
 }
 

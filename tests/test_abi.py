@@ -40,7 +40,8 @@ def test_header_declares_the_entry_points():
     assert names == {"rope_write_kv_packed", "rope_write_kv_continuous", "rope_write_kv_tree",
                      "paged_kv_delta_update", "paged_kv_delta_update_fused",
                      "dflash_prepare_delta_metadata", "dflash_gather_delta_rope",
-                     "rope_check_capacity", "ropekv_status_string"}
+                     "rope_write_kv_slot_mapping", "rope_check_capacity",
+                     "ropekv_status_string"}
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -170,3 +171,24 @@ def test_metadata_and_gather_reject_bad_arguments(lib):
     assert lib.dflash_gather_delta_rope(A, NUL, A, A, NUL, 8, 4, 1, 64, 64, NUL) == ERR["NULL"]
     assert lib.dflash_gather_delta_rope(A, A, A, A, MIS, 8, 4, 1, 64, 64, NUL) == ERR["MISALIGNED"]
     assert lib.dflash_gather_delta_rope(NUL, NUL, NUL, NUL, NUL, 0, 4, 1, 64, 64, NUL) == OK
+
+
+def _slotmap(lib, *, ptrs=None, qs=48 * 128, ks=48 * 128, vs=48 * 128, T=4, Hq=32, Hkv=8, D=128,
+             r=128, rows=16, blocks=4, bsz=16, style=0):
+    p = ptrs or [A] * 10
+    return lib.rope_write_kv_slot_mapping(p[0], p[1], p[2], qs, p[3], ks, p[4], vs, p[5], p[6],
+                                          p[7], p[8], p[9], T, Hq, Hkv, D, r, rows, blocks, bsz,
+                                          style, NUL)
+
+
+def test_slot_mapping_rejects_bad_arguments(lib):
+    assert _slotmap(lib, qs=100) == ERR["SHAPE"]          # smaller than Hq*D
+    assert _slotmap(lib, ks=8 * 128 + 4) == ERR["SHAPE"]   # not a multiple of 8
+    assert _slotmap(lib, bsz=0) == ERR["SHAPE"]
+    assert _slotmap(lib, blocks=-1) == ERR["SHAPE"]
+    assert _slotmap(lib, Hq=12, Hkv=8) == ERR["HEADS"]
+    assert _slotmap(lib, D=96, r=96) == ERR["HEAD_DIM"]
+    assert _slotmap(lib, style=7) == ERR["STYLE"]
+    assert _slotmap(lib, ptrs=[A, A, A, A, A, NUL, A, A, A, A]) == ERR["NULL"]
+    assert _slotmap(lib, ptrs=[A, A, A, A, A, A, A, A, A, MIS]) == ERR["MISALIGNED"]
+    assert _slotmap(lib, T=0, ptrs=[NUL] * 10) == OK

@@ -18,7 +18,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "ropekv_oracle.c")
 HDR = os.path.join(ROOT, "oracle", "ropekv_oracle.h")
 PIN_TESTS = ["tests/test_oracle_rope.py", "tests/test_oracle_entries.py",
-             "tests/test_oracle_dflash.py", "tests/test_oracle_fp16.py"]
+             "tests/test_oracle_dflash.py", "tests/test_oracle_slotmap.py",
+             "tests/test_oracle_fp16.py"]
 
 MUTANTS = {
     "neox_rotate_sign": ("out[d] = (d < h) ? -x[d + h] : x[d - h];",
@@ -58,6 +59,10 @@ MUTANTS = {
     "gather_capacity_unchecked": ("seq < batchSize && pos < cacheCapacity;",
                                   "seq < batchSize && pos <= cacheCapacity;"),
     "gather_shared_row_ignored": ("state = (sourceRows == 1) ? 0 : seq;", "state = seq;"),
+    "slotmap_block_offset_swapped": ("int64_t block = slot / blockSize;\n        int64_t off = slot % blockSize;",
+                                     "int64_t block = slot % blockSize;\n        int64_t off = slot / blockSize;"),
+    "slotmap_negative_slot_written": ("if (slot < 0 || slot >= slots)", "if (slot >= slots)"),
+    "slotmap_stride_ignored": ("rope_head_f16(k + (size_t)t * kStride", "rope_head_f16(k + (size_t)t * Hkv * D"),
 }
 
 

@@ -399,6 +399,93 @@ def make_paged_fused(B, W, Hkv, D, r, tokens_per_page, max_pages_per_seq, num_pa
                           np.ascontiguousarray(table), name=name)
 
 
+# ------------------------------------------------------ flat slot mapping --
+
+@dataclass
+class SlotMapCase:
+    """Inputs of the sglang-style call: q, k, v are views into one packed
+    [T, Hq + 2 Hkv, D] buffer; per-token positions and flat cache slots."""
+    Hq: int
+    Hkv: int
+    D: int
+    r: int
+    style: int
+    theta: float
+    num_blocks: int
+    block_size: int
+    qkv: np.ndarray           # [T, Hq+2Hkv, D] uint16
+    positions: np.ndarray     # [T] int64
+    slots: np.ndarray         # [T] int64
+    cos_sin: np.ndarray       # [rows, r] float32
+    seq_lens: tuple = ()
+    name: str = ""
+
+    @property
+    def T(self) -> int:
+        return self.qkv.shape[0]
+
+    @property
+    def tokens(self) -> int:
+        return self.T
+
+    @property
+    def q(self):
+        return self.qkv[:, : self.Hq]
+
+    @property
+    def k(self):
+        return self.qkv[:, self.Hq: self.Hq + self.Hkv]
+
+    @property
+    def v(self):
+        return self.qkv[:, self.Hq + self.Hkv:]
+
+    def cache_shape(self):
+        return (self.num_blocks, self.block_size, self.Hkv, self.D)
+
+    def algorithmic_bytes(self) -> int:
+        """QKV read + cos/sin read + positions and slots read + Q, K, V written
+        (K and V only for tokens with a valid slot)."""
+        H = self.Hq + 2 * self.Hkv
+        ok = (self.slots >= 0) & (self.slots < self.num_blocks * self.block_size)
+        per_tok = H * self.D * 2 + self.r * 4 + 16 + self.Hq * self.D * 2
+        return int(self.T * per_tok + ok.sum() * 2 * self.Hkv * self.D * 2)
+
+
+def _slot_assignment(rng, seq_lens, block_size, num_blocks):
+    """Each sequence's tokens fill consecutive offsets of its own blocks,
+    starting at a random offset of its first block; blocks come from one
+    random permutation of the pool (no block is shared)."""
+    perm = rng.permutation(num_blocks)
+    nxt = 0
+    out = []
+    for n in seq_lens:
+        first = int(rng.integers(0, block_size))
+        nblk = -(-(first + n) // block_size)
+        blocks = perm[nxt: nxt + nblk]
+        if len(blocks) < nblk:
+            raise ValueError("not enough blocks for the sequences")
+        nxt += nblk
+        idx = first + np.arange(n)
+        out.append(blocks[idx // block_size].astype(np.int64) * block_size + idx % block_size)
+    return np.concatenate(out) if out else np.zeros(0, dtype=np.int64)
+
+
+def make_slotmap(seq_lens, Hq, Hkv, D, r, style, theta, seed, block_size, num_blocks,
+                 start_range, cs_rows, name="slotmap") -> SlotMapCase:
+    rng = rng_for(seed)
+    T = int(sum(seq_lens))
+    qkv = fp16_normal(rng, (T, Hq + 2 * Hkv, D))
+    starts = rng.integers(start_range[0], start_range[1] + 1, size=len(seq_lens))
+    positions = np.concatenate([st + np.arange(n) for st, n in zip(starts, seq_lens)]) \
+        .astype(np.int64) if T else np.zeros(0, dtype=np.int64)
+    slots = _slot_assignment(rng, seq_lens, block_size, num_blocks)
+    cos_sin = cos_sin_table(theta, cs_rows, r)[0]
+    return SlotMapCase(Hq, Hkv, D, r, style, theta, num_blocks, block_size, qkv, positions,
+                       np.ascontiguousarray(slots), np.ascontiguousarray(cos_sin),
+                       tuple(int(x) for x in seq_lens), name=name)
+
+
 # ------------------------------------------------------------ the configs --
 
 CONFIG_NAMES = ("packed_tiny", "prefill", "decode", "tree", "paged")
@@ -409,7 +496,7 @@ CONFIG_NAMES = ("packed_tiny", "prefill", "decode", "tree", "paged")
 PROFILE_NAMES = ("decode_c1024", "paged_p8192")
 
 # Workloads of the next rows (built on the same kernels).
-NEXT_NAMES = ("paged_fused",)
+NEXT_NAMES = ("paged_fused", "slotmap_prefill", "slotmap_decode")
 
 
 def config(name: str):
@@ -447,6 +534,15 @@ def config(name: str):
     if name == "paged_p8192":
         return make_paged(16384, 128, 8, 128, 128, 64, 64, 8192, NEOX, 5e5, seed=4,
                           valid_rows=15565, name=name)
+    if name == "slotmap_prefill":
+        # the prefill above behind the sglang-style interface: 4 x 2048 tokens,
+        # block size 64, 16384 blocks per cache, positions from start in [0, 4096]
+        return make_slotmap([2048] * 4, 32, 8, 128, 128, NEOX, 5e5, seed=6, block_size=64,
+                            num_blocks=16384, start_range=(0, 4096), cs_rows=8192, name=name)
+    if name == "slotmap_decode":
+        # 256 one-token sequences at positions in [0, 8191], one slot each
+        return make_slotmap([1] * 256, 32, 8, 128, 128, NEOX, 5e5, seed=7, block_size=64,
+                            num_blocks=16384, start_range=(0, 8191), cs_rows=8192, name=name)
     if name == "paged_fused":
         # the DFlash step in one launch: B=128 sequences x deltaWidth 128 rows
         # (16384 rows), delta lengths uniform in [1, 128], Hkv=8, D=r=128,
@@ -474,6 +570,15 @@ def step_variant(case, k: int):
     every step writes different pages. Fused DFlash cases: (old_lengths,
     page_table).
     """
+    if isinstance(case, SlotMapCase):
+        if k == 0:
+            return case.positions, case.slots
+        rng = rng_for(1000 + k)
+        lo, hi = int(case.positions.min()), int(case.positions.max())
+        starts = rng.integers(0, max(1, hi - lo + 1), size=len(case.seq_lens))
+        pos = np.concatenate([lo + st + np.arange(n) for st, n in zip(starts, case.seq_lens)])
+        slots = _slot_assignment(rng, case.seq_lens, case.block_size, case.num_blocks)
+        return pos.astype(np.int64), np.ascontiguousarray(slots)
     if k == 0:
         if isinstance(case, PagedCase):
             return case.page_table
