@@ -41,7 +41,7 @@ import workloads  # noqa: E402
 METRIC = "fused RoPE+KV-write tokens/s and effective HBM GB/s (% of GB300 peak)"
 HEADLINE = "prefill"
 EXTRA = ("decode", "tree", "paged", "packed_tiny", "paged_fused", "paged_fused_3launch",
-         "slotmap_prefill", "slotmap_decode")
+         "slotmap_prefill", "slotmap_decode", "prefill_qknorm", "decode_qknorm")
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 
@@ -63,6 +63,8 @@ DESCR = {
                        "packed buffer, per-token positions and flat slots, block size 64, "
                        "16384 blocks",
     "slotmap_decode": "256 one-token decodes behind the sglang-style interface",
+    "prefill_qknorm": "the prefill with pre-RoPE QK RMS norm fused in (weights [128], eps 1e-6)",
+    "decode_qknorm": "the decode with pre-RoPE QK RMS norm fused in (weights [128], eps 1e-6)",
     "decode_c1024": "decode as above with cache capacity 1024 (profiler-sized twin)",
     "paged_p8192": "paged as above with 64 pages/seq and 8192 pages per plane (profiler-sized twin)",
 }
@@ -240,6 +242,9 @@ class DeviceWorkload:
                                       slots=t(slots), qout=self._sentinel((c.T, c.Hq, c.D))))
         else:
             self.cos_sin = t(c.cos_sin)
+            self.norm = None
+            if c.norm is not None:
+                self.norm = (t(c.norm[0]), t(c.norm[1]), float(c.norm[2]))
             self.cache = (t(c.new_cache()) if c.cache_init == "zero"
                           else self._sentinel((c.B, 2, c.Hkv, c.cap, c.D)))
             qkv_base = t(c.qkv)
@@ -311,6 +316,11 @@ class DeviceWorkload:
         elif c.mode == "tree":
             rk.rope_write_kv_tree(self.cos_sin, s["end"], s["pos"], s["qkv"], self.cache,
                                   s["qout"], c.Hq, c.Hkv, c.style, stream=stream)
+        elif self.norm is not None:
+            qw, kw, eps = self.norm
+            rk.rope_write_kv_continuous_qknorm(self.cos_sin, s["end"], s["qkv"], self.cache,
+                                               s["qout"], qw, kw, eps, c.Hq, c.Hkv, c.style,
+                                               stream=stream)
         else:
             rk.rope_write_kv_continuous(self.cos_sin, s["end"], s["qkv"], self.cache, s["qout"],
                                         c.Hq, c.Hkv, c.style, stream=stream)
@@ -663,7 +673,7 @@ def _kernel_name(wl) -> str:
     if wl.paged:
         return f"paged_delta_kernel<D={c.D}, {'NeoX' if c.style == 0 else 'GPT-J'}>"
     return (f"rope_kv_token_kernel<D={c.D}, {'NeoX' if c.style == 0 else 'GPT-J'}, "
-            f"{c.mode}>")
+            f"{c.mode}{', qk-norm' if c.norm is not None else ''}>")
 
 
 if __name__ == "__main__":

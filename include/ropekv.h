@@ -13,6 +13,8 @@
  *   [DRK] TensorRT-Edge-LLM C++ API, "Dflash Runtime Kernels"
  *         (launchDFlashTargetKVCacheUpdate, checkDFlashRopeCapacity,
  *         launchDFlashPrepareDeltaMetadata, launchDFlashGatherDeltaRope).
+ *   [MIR] libmir-cuda 0.1.0 backend/attention/graph/execution.rs (qkv_postprocess:
+ *         QK normalization before RoPE, then the KV store).
  *   [RC]  sglang rope_cache.py (_get_neox_rotated_x, _get_gptj_rotated_x,
  *         _unit_rope, _load_cos_sin, kernel Stage 2.1; the
  *         fused_qk_rope_reshape_and_cache interface, Stages 3.1-3.5).
@@ -117,6 +119,25 @@ ROPEKV_API int rope_write_kv_continuous(const float* cosSin, const int32_t* kvCa
                                         const uint16_t* qkv, uint16_t* kvCache,
                                         uint16_t* qOut, const ropekv_dims* dims,
                                         void* stream);
+
+/*
+ * rope_write_kv_continuous with pre-RoPE RMS normalization of Q and K fused in
+ * (libmir-cuda execution.rs: qkv_postprocess normalizes Q and K with
+ * query_norm / key_norm weights and an epsilon before RoPE, then the KV store
+ * runs; "Dflash Runtime Kernels" calls its K input "k_normed"). Every Q head x
+ * becomes x[d] / sqrt(mean_d' x[d']^2 + eps) * qNormWeight[d] (K heads with
+ * kNormWeight), in FP32, before the rotation; the result is rounded to FP16
+ * once. V is copied as bits. Dims >= rotaryDim of Q and K are normalized too.
+ *   qNormWeight, kNormWeight  [headDim] FP16, read.
+ *   eps                       >= 0.
+ * Everything else as rope_write_kv_continuous.
+ */
+ROPEKV_API int rope_write_kv_continuous_qknorm(const float* cosSin,
+                                               const int32_t* kvCacheEndLens,
+                                               const uint16_t* qkv, uint16_t* kvCache,
+                                               uint16_t* qOut, const uint16_t* qNormWeight,
+                                               const uint16_t* kNormWeight, float eps,
+                                               const ropekv_dims* dims, void* stream);
 
 /*
  * [ARW] launchApplyRopeWriteKVTreeDecoding: tree attention for speculative

@@ -96,6 +96,16 @@ def _load():
     lib.ropekv_oracle_gather_delta_rope.restype = I
     lib.ropekv_oracle_paged_fused.argtypes = [P] * 9 + [I] * 10
     lib.ropekv_oracle_paged_fused.restype = I
+    lib.ropekv_oracle_continuous_qknorm.argtypes = [P] * 7 + [ctypes.c_float] + [I] * 10
+    lib.ropekv_oracle_continuous_qknorm.restype = I
+    lib.ropekv_oracle_rms_norm_f64.argtypes = [P, P, ctypes.c_double, I, P]
+    lib.ropekv_oracle_rms_norm_f64.restype = None
+    lib.ropekv_oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+    lib.ropekv_oracle_e4m3_to_f64.restype = ctypes.c_double
+    lib.ropekv_oracle_f64_to_e4m3.argtypes = [ctypes.c_double]
+    lib.ropekv_oracle_f64_to_e4m3.restype = ctypes.c_uint8
+    lib.ropekv_oracle_continuous_fp8.argtypes = [P] * 5 + [ctypes.c_float] * 2 + [I] * 10
+    lib.ropekv_oracle_continuous_fp8.restype = I
     L = ctypes.c_int64
     lib.ropekv_oracle_slot_mapping.argtypes = [P, P, P, L, P, L, P, L, P, P, P, P, P,
                                                I, I, I, I, I, I, L, I, I]
@@ -192,6 +202,53 @@ def continuous(cos_sin, end_lens, qkv, kv_cache, q_out, Hq, Hkv, style):
                                           _ptr(q_out, np.uint16),
                                           B, S, Hq, Hkv, D, r, cap, csB, csS, style)
     _check(rc, "continuous")
+
+
+def continuous_qknorm(cos_sin, end_lens, qkv, kv_cache, q_out, q_weight, k_weight, eps, Hq, Hkv,
+                      style):
+    """Continuous path with pre-RoPE RMS normalization of Q and K heads
+    (weights: [D] uint16 FP16 bits). Mutates ``kv_cache`` and ``q_out``."""
+    csB, csS, r = cos_sin.shape
+    B, S, H, D = qkv.shape
+    cap = kv_cache.shape[3]
+    assert H == Hq + 2 * Hkv and kv_cache.shape == (B, 2, Hkv, cap, D)
+    assert q_weight.shape == (D,) and k_weight.shape == (D,)
+    rc = _load().ropekv_oracle_continuous_qknorm(
+        _ptr(cos_sin, np.float32), _ptr(end_lens, np.int32), _ptr(qkv, np.uint16),
+        _ptr(kv_cache, np.uint16), _ptr(q_out, np.uint16), _ptr(q_weight, np.uint16),
+        _ptr(k_weight, np.uint16), float(eps), B, S, Hq, Hkv, D, r, cap, csB, csS, style)
+    _check(rc, "continuous_qknorm")
+
+
+def e4m3_to_f64(bits: int) -> float:
+    return _load().ropekv_oracle_e4m3_to_f64(int(bits) & 0xFF)
+
+
+def f64_to_e4m3(x: float) -> int:
+    return int(_load().ropekv_oracle_f64_to_e4m3(float(x)))
+
+
+def continuous_fp8(cos_sin, end_lens, qkv, kv_cache8, q_out, k_scale, v_scale, Hq, Hkv, style):
+    """Continuous call with an E4M3 cache (uint8 [B, 2, Hkv, cap, D]). Mutates
+    ``kv_cache8`` and ``q_out``."""
+    csB, csS, r = cos_sin.shape
+    B, S, H, D = qkv.shape
+    cap = kv_cache8.shape[3]
+    assert H == Hq + 2 * Hkv and kv_cache8.shape == (B, 2, Hkv, cap, D)
+    rc = _load().ropekv_oracle_continuous_fp8(
+        _ptr(cos_sin, np.float32), _ptr(end_lens, np.int32), _ptr(qkv, np.uint16),
+        _ptr(kv_cache8, np.uint8), _ptr(q_out, np.uint16), float(k_scale), float(v_scale),
+        B, S, Hq, Hkv, D, r, cap, csB, csS, style)
+    _check(rc, "continuous_fp8")
+
+
+def rms_norm_f64(x, weight, eps):
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    weight = np.ascontiguousarray(weight, dtype=np.uint16)
+    y = np.zeros_like(x)
+    _load().ropekv_oracle_rms_norm_f64(_ptr(x, np.float64), _ptr(weight, np.uint16), float(eps),
+                                       x.shape[0], _ptr(y, np.float64))
+    return y
 
 
 def tree(cos_sin, end_lens, pos_ids, qkv, kv_cache, q_out, Hq, Hkv, style):

@@ -69,6 +69,53 @@ uint16_t ropekv_oracle_f64_to_f16(double x)
     return (uint16_t)(sign | (uint16_t)((E + 15) << 10) | (uint16_t)(q - 1024.0));
 }
 
+/* ---------------------------------------------------------------- FP8 ----- */
+
+/* E4M3: exponent field 0 is subnormal, value = fraction * 2^-9; otherwise
+ * value = (8 + fraction) * 2^(exponent - 10); S.1111.111 is NaN. */
+double ropekv_oracle_e4m3_to_f64(uint8_t bits)
+{
+    int sign = (bits >> 7) & 1;
+    int e = (bits >> 3) & 0xF;
+    int f = bits & 0x7;
+    double v;
+    if (e == 15 && f == 7)
+        return NAN;
+    if (e == 0)
+        v = ldexp((double)f, -9);
+    else
+        v = ldexp((double)(8 + f), e - 10);
+    return sign ? -v : v;
+}
+
+uint8_t ropekv_oracle_f64_to_e4m3(double x)
+{
+    if (isnan(x))
+        return 0x7F;
+    uint8_t sign = signbit(x) ? 0x80u : 0u;
+    double a = fabs(x);
+    if (isinf(a)) /* saturates like any magnitude above 448 */
+        return (uint8_t)(sign | 0x7E);
+    if (a < ldexp(1.0, -6)) {
+        /* subnormals: multiples of 2^-9; 8 * 2^-9 is the smallest normal 0x08 */
+        double k = nearbyint(ldexp(a, 9));
+        return (uint8_t)(sign | (uint8_t)k);
+    }
+    int E;
+    (void)frexp(a, &E);
+    E -= 1; /* 2^E <= a < 2^(E+1) */
+    double q = nearbyint(ldexp(a, 3 - E)); /* significand * 8, in [8, 16] */
+    if (q == 16.0) {
+        q = 8.0;
+        E += 1;
+    }
+    int field = E + 7;
+    /* saturate: 448 = S.1111.110 is the largest finite value, S.1111.111 is NaN */
+    if (field > 15 || (field == 15 && q - 8.0 > 6.0))
+        return (uint8_t)(sign | 0x7E);
+    return (uint8_t)(sign | (uint8_t)(field << 3) | (uint8_t)(q - 8.0));
+}
+
 /* ---------------------------------------------------------------- RoPE ---- */
 
 void ropekv_oracle_rotate_half(const double* x, int r, int style, double* out)
@@ -420,6 +467,112 @@ int ropekv_oracle_paged_fused(const uint16_t* kDelta, const uint16_t* vDelta, ui
     free(seq);
     free(pos);
     return rc;
+}
+
+void ropekv_oracle_rms_norm_f64(const double* x, const uint16_t* weight, double eps, int D,
+                                double* y)
+{
+    double ss = 0.0;
+    for (int d = 0; d < D; ++d)
+        ss += x[d] * x[d];
+    double inv = 1.0 / sqrt(ss / D + eps);
+    for (int d = 0; d < D; ++d)
+        y[d] = x[d] * inv * ropekv_oracle_f16_to_f64(weight[d]);
+}
+
+/* Normalize one FP16 head, rotate it and round every dim to FP16. */
+static void norm_rope_head_f16(const uint16_t* src, const uint16_t* weight, double eps,
+                               const float* cs, int D, int r, int style, uint16_t* dst)
+{
+    double* x = (double*)calloc((size_t)D, sizeof(double));
+    double* n = (double*)calloc((size_t)D, sizeof(double));
+    double* y = (double*)calloc((size_t)D, sizeof(double));
+    for (int d = 0; d < D; ++d)
+        x[d] = ropekv_oracle_f16_to_f64(src[d]);
+    ropekv_oracle_rms_norm_f64(x, weight, eps, D, n);
+    ropekv_oracle_rope_head_f64(n, cs, D, r, style, y);
+    for (int d = 0; d < D; ++d)
+        dst[d] = ropekv_oracle_f64_to_f16(y[d]);
+    free(y);
+    free(n);
+    free(x);
+}
+
+int ropekv_oracle_continuous_qknorm(const float* cosSin, const int32_t* kvCacheEndLens,
+                                    const uint16_t* qkv, uint16_t* kvCache, uint16_t* qOut,
+                                    const uint16_t* qNormWeight, const uint16_t* kNormWeight,
+                                    float eps, int B, int S, int Hq, int Hkv, int D, int r,
+                                    int cap, int csBatch, int csSeq, int style)
+{
+    if (!dims_ok(B, S, Hq, Hkv, D, r, cap, csBatch, csSeq, style))
+        return -1;
+    int H = Hq + 2 * Hkv;
+    for (int b = 0; b < B; ++b) {
+        for (int s = 0; s < S; ++s) {
+            /* slot = position = end - S + s, as in the continuous call */
+            long long pos = (long long)kvCacheEndLens[b] - S + s;
+            long long slot = pos;
+            if (slot < 0 || slot >= cap || pos >= csSeq)
+                continue;
+            const uint16_t* tok = qkv + qkv_at(b, s, 0, S, H, D);
+            const float* cs = cs_row_at(cosSin, b, (int)pos, csBatch, csSeq, r);
+            for (int hq = 0; hq < Hq; ++hq)
+                norm_rope_head_f16(tok + (size_t)hq * D, qNormWeight, (double)eps, cs, D, r,
+                                   style, qOut + qout_at(b, s, hq, S, Hq, D));
+            for (int hk = 0; hk < Hkv; ++hk)
+                norm_rope_head_f16(tok + (size_t)(Hq + hk) * D, kNormWeight, (double)eps, cs, D,
+                                   r, style, kvCache + cache_at(b, 0, hk, (int)slot, Hkv, cap, D));
+            for (int hv = 0; hv < Hkv; ++hv)
+                memcpy(kvCache + cache_at(b, 1, hv, (int)slot, Hkv, cap, D),
+                       tok + (size_t)(Hq + Hkv + hv) * D, sizeof(uint16_t) * (size_t)D);
+        }
+    }
+    return 0;
+}
+
+int ropekv_oracle_continuous_fp8(const float* cosSin, const int32_t* kvCacheEndLens,
+                                 const uint16_t* qkv, uint8_t* kvCache8, uint16_t* qOut,
+                                 float kScale, float vScale, int B, int S, int Hq, int Hkv, int D,
+                                 int r, int cap, int csBatch, int csSeq, int style)
+{
+    if (!dims_ok(B, S, Hq, Hkv, D, r, cap, csBatch, csSeq, style) || !(kScale > 0.0f) ||
+        !(vScale > 0.0f))
+        return -1;
+    int H = Hq + 2 * Hkv;
+    double* x = (double*)calloc((size_t)D, sizeof(double));
+    double* y = (double*)calloc((size_t)D, sizeof(double));
+    for (int b = 0; b < B; ++b) {
+        for (int s = 0; s < S; ++s) {
+            /* slots and positions exactly as the continuous call */
+            long long end = kvCacheEndLens[b];
+            long long slot = end - S + s;
+            if (slot < 0 || slot >= cap || slot >= csSeq)
+                continue;
+            const uint16_t* tok = qkv + qkv_at(b, s, 0, S, H, D);
+            const float* cs = cs_row_at(cosSin, b, (int)slot, csBatch, csSeq, r);
+            for (int hq = 0; hq < Hq; ++hq)
+                rope_head_f16(tok + (size_t)hq * D, cs, D, r, style,
+                              qOut + qout_at(b, s, hq, S, Hq, D));
+            for (int hk = 0; hk < Hkv; ++hk) {
+                for (int d = 0; d < D; ++d)
+                    x[d] = ropekv_oracle_f16_to_f64(tok[(size_t)(Hq + hk) * D + d]);
+                ropekv_oracle_rope_head_f64(x, cs, D, r, style, y);
+                uint8_t* kc = kvCache8 + cache_at(b, 0, hk, (int)slot, Hkv, cap, D);
+                for (int d = 0; d < D; ++d)
+                    kc[d] = ropekv_oracle_f64_to_e4m3(y[d] * (1.0 / (double)kScale));
+            }
+            for (int hv = 0; hv < Hkv; ++hv) {
+                const uint16_t* vsrc = tok + (size_t)(Hq + Hkv + hv) * D;
+                uint8_t* vc = kvCache8 + cache_at(b, 1, hv, (int)slot, Hkv, cap, D);
+                for (int d = 0; d < D; ++d)
+                    vc[d] = ropekv_oracle_f64_to_e4m3(ropekv_oracle_f16_to_f64(vsrc[d]) *
+                                                      (1.0 / (double)vScale));
+            }
+        }
+    }
+    free(y);
+    free(x);
+    return 0;
 }
 
 int ropekv_oracle_slot_mapping(const float* cosSin, const int64_t* positions,

@@ -150,6 +150,42 @@ int ropekv_oracle_paged_fused(const uint16_t* kDelta, const uint16_t* vDelta, ui
                               int maxPagesPerSeq, int tokensPerPage, int sourceRows,
                               int cacheCapacity, int style);
 
+/* Pre-RoPE QK RMS normalization fused into the continuous call (libmir-cuda
+ * execution.rs: qkv_postprocess normalizes Q and K with query_norm / key_norm
+ * weights and epsilon, then applies RoPE, then the KV store; "Dflash Runtime
+ * Kernels": kDelta is "k_normed, no RoPE"). Reading: each Q head x [D] becomes
+ *   x_hat[d] = x[d] / sqrt(mean_{d'} x[d']^2 + eps) * qNormWeight[d]
+ * (K heads with kNormWeight), then RoPE on x_hat, rounded to FP16 once; V is
+ * copied as bits. Weights are FP16 [D]. Placement and skips: as the continuous
+ * call. Dims >= r of Q and K are normalized (no longer bit copies). */
+int ropekv_oracle_continuous_qknorm(const float* cosSin, const int32_t* kvCacheEndLens,
+                                    const uint16_t* qkv, uint16_t* kvCache, uint16_t* qOut,
+                                    const uint16_t* qNormWeight, const uint16_t* kNormWeight,
+                                    float eps, int B, int S, int Hq, int Hkv, int D, int r,
+                                    int cap, int csBatch, int csSeq, int style);
+
+/* RMS normalization of one head in double (the first step above). */
+void ropekv_oracle_rms_norm_f64(const double* x, const uint16_t* weight, double eps, int D,
+                                double* y);
+
+/* OCP FP8 E4M3 ("e4m3fn": 4 exponent bits, bias 7, 3 fraction bits, no
+ * infinities, 0x7F / 0xFF NaN, largest finite 448) bits -> double (exact). */
+double ropekv_oracle_e4m3_to_f64(uint8_t bits);
+
+/* double -> E4M3 bits: round to nearest, ties to even; magnitudes above 448
+ * (and infinities) saturate to +-448; NaN -> 0x7F. */
+uint8_t ropekv_oracle_f64_to_e4m3(double x);
+
+/* The continuous call with an FP8 cache ([RC] kernel Stage 3.3: K and V are
+ * multiplied by 1/k_scale and 1/v_scale before the cache store, which converts
+ * them to the cache's FP8 type). kvCache8 [B, 2, Hkv, cap, D] holds E4M3 bytes:
+ * plane 0 = e4m3(rope(K) / kScale), plane 1 = e4m3(V / vScale); rotated Q goes
+ * to qOut in FP16 as in the continuous call. */
+int ropekv_oracle_continuous_fp8(const float* cosSin, const int32_t* kvCacheEndLens,
+                                 const uint16_t* qkv, uint8_t* kvCache8, uint16_t* qOut,
+                                 float kScale, float vScale, int B, int S, int Hq, int Hkv, int D,
+                                 int r, int cap, int csBatch, int csSeq, int style);
+
 /* [RC] fused_qk_rope_reshape_and_cache with the flash cache layout.
  * Token t (of T) has RoPE position positions[t] (row of cosSin [cosSinRows, r])
  * and flat cache slot slotMapping[t]. Q [T, Hq, D], K and V [T, Hkv, D] are read

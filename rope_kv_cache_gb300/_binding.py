@@ -59,6 +59,7 @@ def load_library():
     lib.rope_write_kv_packed.argtypes = [P, P, P, D, P]
     lib.rope_write_kv_continuous.argtypes = [P, P, P, P, P, D, P]
     lib.rope_write_kv_tree.argtypes = [P, P, P, P, P, P, D, P]
+    lib.rope_write_kv_continuous_qknorm.argtypes = [P, P, P, P, P, P, P, ctypes.c_float, D, P]
     lib.paged_kv_delta_update.argtypes = [P] * 7 + [I32] * 9 + [P]
     lib.paged_kv_delta_update_fused.argtypes = [P] * 6 + [I32] + [P] * 2 + [I32] * 10 + [P]
     lib.dflash_prepare_delta_metadata.argtypes = [P, P, I32, P, P, I32, P]
@@ -70,6 +71,7 @@ def load_library():
     lib.ropekv_status_string.argtypes = [ctypes.c_int]
     lib.ropekv_status_string.restype = ctypes.c_char_p
     for fn in ("rope_write_kv_packed", "rope_write_kv_continuous", "rope_write_kv_tree",
+               "rope_write_kv_continuous_qknorm",
                "paged_kv_delta_update", "paged_kv_delta_update_fused",
                "dflash_prepare_delta_metadata", "dflash_gather_delta_rope",
                "rope_write_kv_slot_mapping", "rope_check_capacity"):
@@ -186,6 +188,30 @@ def rope_write_kv_continuous(cos_sin: torch.Tensor, kv_cache_end_lens: torch.Ten
         _dev_ptr(qkv, "qkv", _F16, dev), _dev_ptr(kv_cache, "kv_cache", _F16, dev),
         _dev_ptr(q_out, "q_out", _F16, dev), ctypes.byref(dims), _stream_handle(stream, dev))
     _check_rc("rope_write_kv_continuous", rc)
+
+
+def rope_write_kv_continuous_qknorm(cos_sin: torch.Tensor, kv_cache_end_lens: torch.Tensor,
+                                    qkv: torch.Tensor, kv_cache: torch.Tensor, q_out: torch.Tensor,
+                                    q_norm_weight: torch.Tensor, k_norm_weight: torch.Tensor,
+                                    eps: float, num_q_heads: int, num_kv_heads: int,
+                                    style: int = NEOX,
+                                    stream: Optional[torch.cuda.Stream] = None) -> None:
+    """rope_write_kv_continuous with per-head RMS normalization of Q and K
+    (weights [D] float16) before the rotation."""
+    dims = _contiguous_dims(cos_sin, qkv, kv_cache, num_q_heads, num_kv_heads, style)
+    B, S, _, D = qkv.shape
+    if tuple(kv_cache_end_lens.shape) != (B,) or tuple(q_out.shape) != (B, S, num_q_heads, D) \
+            or tuple(q_norm_weight.shape) != (D,) or tuple(k_norm_weight.shape) != (D,):
+        raise ValueError("kv_cache_end_lens [B], q_out [B,S,Hq,D], norm weights [D] expected")
+    dev = qkv.device
+    rc = load_library().rope_write_kv_continuous_qknorm(
+        _dev_ptr(cos_sin, "cos_sin", _F32, dev),
+        _dev_ptr(kv_cache_end_lens, "kv_cache_end_lens", _I32, dev),
+        _dev_ptr(qkv, "qkv", _F16, dev), _dev_ptr(kv_cache, "kv_cache", _F16, dev),
+        _dev_ptr(q_out, "q_out", _F16, dev), _dev_ptr(q_norm_weight, "q_norm_weight", _F16, dev),
+        _dev_ptr(k_norm_weight, "k_norm_weight", _F16, dev), float(eps), ctypes.byref(dims),
+        _stream_handle(stream, dev))
+    _check_rc("rope_write_kv_continuous_qknorm", rc)
 
 
 def rope_write_kv_tree(cos_sin: torch.Tensor, kv_cache_end_lens: torch.Tensor,

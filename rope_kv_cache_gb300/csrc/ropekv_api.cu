@@ -75,7 +75,12 @@ template <int D, int STYLE, int MODE, int IPT>
 void launch_token(const TokenArgs& a, long long tokens, const Shape& sh, cudaStream_t st)
 {
     const unsigned grid = (unsigned)(tokens * sh.ctasPerUnit);
-    ropekv::rope_kv_token_kernel<D, STYLE, MODE, IPT, kPolicy><<<grid, sh.threads, 0, st>>>(a);
+    if (MODE == ropekv::kContinuous && a.qNormW != nullptr)
+        ropekv::rope_kv_token_kernel<D, STYLE, MODE, IPT, kPolicy, true>
+            <<<grid, sh.threads, 0, st>>>(a);
+    else
+        ropekv::rope_kv_token_kernel<D, STYLE, MODE, IPT, kPolicy, false>
+            <<<grid, sh.threads, 0, st>>>(a);
 }
 
 template <int D, int STYLE, int MODE>
@@ -278,6 +283,37 @@ int rope_write_kv_continuous(const float* cosSin, const int32_t* kvCacheEndLens,
     a.qkv = qkv;
     a.cache = kvCache;
     a.qOut = qOut;
+    return launch_contiguous(a, dims, tokens, ropekv::kContinuous, (cudaStream_t)stream);
+}
+
+int rope_write_kv_continuous_qknorm(const float* cosSin, const int32_t* kvCacheEndLens,
+                                    const uint16_t* qkv, uint16_t* kvCache, uint16_t* qOut,
+                                    const uint16_t* qNormWeight, const uint16_t* kNormWeight,
+                                    float eps, const ropekv_dims* dims, void* stream)
+{
+    long long tokens = 0;
+    int rc = check_dims(dims, &tokens);
+    if (rc != ROPEKV_OK)
+        return rc;
+    if (!(eps >= 0.0f) || eps > 1.0e30f)
+        return ROPEKV_ERR_SHAPE;
+    if (tokens == 0)
+        return ROPEKV_OK;
+    if (!cosSin || !kvCacheEndLens || !qkv || !kvCache || !qOut || !qNormWeight || !kNormWeight)
+        return ROPEKV_ERR_NULL_POINTER;
+    if (!aligned16(cosSin) || !aligned16(kvCacheEndLens) || !aligned16(qkv) ||
+        !aligned16(kvCache) || !aligned16(qOut) || !aligned16(qNormWeight) ||
+        !aligned16(kNormWeight))
+        return ROPEKV_ERR_MISALIGNED;
+    TokenArgs a = token_args(dims);
+    a.cosSin = cosSin;
+    a.endLens = kvCacheEndLens;
+    a.qkv = qkv;
+    a.cache = kvCache;
+    a.qOut = qOut;
+    a.qNormW = qNormWeight;
+    a.kNormW = kNormWeight;
+    a.eps = eps;
     return launch_contiguous(a, dims, tokens, ropekv::kContinuous, (cudaStream_t)stream);
 }
 

@@ -46,6 +46,9 @@ struct TokenArgs {
     uint16_t* qkvOut;          // same buffer as qkv for the packed in-place call
     uint16_t* cache;           // [B, 2, Hkv, cap, D]
     uint16_t* qOut;            // [B, S, Hq, D] (continuous, tree)
+    const uint16_t* qNormW;    // [D] FP16 RMS-norm weight of Q heads (normalized call)
+    const uint16_t* kNormW;    // [D] FP16 RMS-norm weight of K heads (normalized call)
+    float eps;                 // RMS-norm epsilon (normalized call)
     int32_t S, Hq, Hkv, r, cap, csBatch, csSeq;
     int32_t itemsPerToken;     // (Hq + 2 Hkv) * D / 16
     int32_t ctasPerToken;      // CTAs sharing one token's items
@@ -280,6 +283,54 @@ __device__ __forceinline__ void rotate_gptj(uint4& v, const float* c, const floa
     }
 }
 
+// Unpack / pack 8 FP16 values of a 16-byte vector to / from FP32.
+__device__ __forceinline__ void unpack8(uint4 v, float f[8])
+{
+    uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float2 x = __half22float2(h2(w[k]));
+        f[2 * k] = x.x;
+        f[2 * k + 1] = x.y;
+    }
+}
+
+__device__ __forceinline__ uint4 pack8(const float f[8])
+{
+    uint4 v;
+    uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        h2(w[k]) = __floats2half2_rn(f[2 * k], f[2 * k + 1]);
+    return v;
+}
+
+// The rotation of rotate_item on FP32 values (fa, fb: the item's two vectors).
+template <int STYLE>
+__device__ __forceinline__ void rotate_item_f32(float fa[8], float fb[8], const float c[8],
+                                                const float s[8])
+{
+    if (STYLE == kNeox) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const float x = fa[k], y = fb[k];
+            fa[k] = fmaf(x, c[k], -(y * s[k]));
+            fb[k] = fmaf(y, c[k], x * s[k]);
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            float e = fa[2 * j], o = fa[2 * j + 1];
+            fa[2 * j] = fmaf(e, c[j], -(o * s[j]));
+            fa[2 * j + 1] = fmaf(o, c[j], e * s[j]);
+            e = fb[2 * j];
+            o = fb[2 * j + 1];
+            fb[2 * j] = fmaf(e, c[4 + j], -(o * s[4 + j]));
+            fb[2 * j + 1] = fmaf(o, c[4 + j], e * s[4 + j]);
+        }
+    }
+}
+
 template <int STYLE>
 __device__ __forceinline__ void rotate_item(uint4& va, uint4& vb, const float c[8],
                                             const float s[8])
@@ -297,7 +348,13 @@ __device__ __forceinline__ void rotate_item(uint4& va, uint4& vb, const float c[
 // Grid: tokens * ctasPerToken CTAs; CTA (token, part) covers items
 // [part * blockDim * IPT, (part + 1) * blockDim * IPT) of the token, each thread
 // items tid + k * blockDim for k < IPT. blockDim is a multiple of D/16.
-template <int D, int STYLE, int MODE, int IPT, int POL>
+//
+// NORM (continuous only): every Q and K head is first RMS-normalized over its D
+// dims with its weight vector, x * rsqrt(mean(x^2) + eps) * w, in FP32, then
+// rotated, then rounded once. A head's D/16 items sit in D/16 consecutive lanes
+// of one warp (items are head-major and blocks are whole warps), so the sum of
+// squares is one xor-shuffle reduction over those lanes.
+template <int D, int STYLE, int MODE, int IPT, int POL, bool NORM = false>
 __global__ void __launch_bounds__(256) rope_kv_token_kernel(const TokenArgs a)
 {
     constexpr int kItemsPerHead = D / 16;
@@ -316,7 +373,7 @@ __global__ void __launch_bounds__(256) rope_kv_token_kernel(const TokenArgs a)
 
     // 1. this thread's QKV vectors (independent of the position chain)
     const uint16_t* tokIn = a.qkv + (size_t)tok * H * D;
-    uint4 xa[IPT], xb[IPT];
+    uint4 xa[IPT] = {}, xb[IPT] = {};
 #pragma unroll
     for (int k = 0; k < IPT; ++k) {
         const int item = item0 + k * blockDim.x;
@@ -354,6 +411,47 @@ __global__ void __launch_bounds__(256) rope_kv_token_kernel(const TokenArgs a)
         load_cos_sin<STYLE, POL>(row, i, a.r, c, sn, pol);
     }
 
+    if (NORM) {
+        // weights of this lane's 16 dims, for Q heads and for K heads
+        float wq[16], wk[16];
+        unpack8(__ldg(reinterpret_cast<const uint4*>(a.qNormW + 8 * va)), wq);
+        unpack8(__ldg(reinterpret_cast<const uint4*>(a.qNormW + 8 * vb)), wq + 8);
+        unpack8(__ldg(reinterpret_cast<const uint4*>(a.kNormW + 8 * va)), wk);
+        unpack8(__ldg(reinterpret_cast<const uint4*>(a.kNormW + 8 * vb)), wk + 8);
+#pragma unroll
+        for (int k = 0; k < IPT; ++k) {
+            const int item = item0 + k * blockDim.x;
+            const int head = item / kItemsPerHead;
+            const bool qk = item < a.itemsPerToken && head < a.Hq + a.Hkv;
+            float fa[8], fb[8];
+            unpack8(xa[k], fa);
+            unpack8(xb[k], fb);
+            float ss = 0.0f;
+            if (qk) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    ss = fmaf(fa[j], fa[j], fmaf(fb[j], fb[j], ss));
+            }
+            // all lanes take part: a head's lanes are aligned groups of D/16
+#pragma unroll
+            for (int off = 1; off < kItemsPerHead; off <<= 1)
+                ss += __shfl_xor_sync(0xffffffffu, ss, off);
+            if (!qk)
+                continue;
+            const float inv = rsqrtf(ss * (1.0f / D) + a.eps);
+            const float* w = head < a.Hq ? wq : wk;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                fa[j] = fa[j] * inv * w[j];
+                fb[j] = fb[j] * inv * w[8 + j];
+            }
+            if (rotItem)
+                rotate_item_f32<STYLE>(fa, fb, c, sn);
+            xa[k] = pack8(fa);
+            xb[k] = pack8(fb);
+        }
+    }
+
     // 4. rotate and store
 #pragma unroll
     for (int k = 0; k < IPT; ++k) {
@@ -363,7 +461,7 @@ __global__ void __launch_bounds__(256) rope_kv_token_kernel(const TokenArgs a)
         const int head = item / kItemsPerHead;
         uint16_t* dst;
         if (head < a.Hq + a.Hkv) {
-            if (rotItem)
+            if (!NORM && rotItem)
                 rotate_item<STYLE>(xa[k], xb[k], c, sn);
             if (head < a.Hq) {
                 dst = (MODE == kPacked) ? a.qkvOut + (size_t)tok * H * D + (size_t)head * D
@@ -435,7 +533,7 @@ __global__ void __launch_bounds__(256) paged_delta_kernel(const PagedArgs a)
 
     // delta rows (issued before the page-table lookups resolve)
     const size_t rowOff = (size_t)t * a.Hkv * D;
-    uint4 xa[IPT], xb[IPT];
+    uint4 xa[IPT] = {}, xb[IPT] = {};
 #pragma unroll
     for (int k = 0; k < IPT; ++k) {
         const int item = item0 + k * blockDim.x;
@@ -520,7 +618,7 @@ __global__ void __launch_bounds__(256) rope_kv_slotmap_kernel(const SlotMapArgs 
     int va, vb;
     item_vectors<D>(i, a.r, va, vb);
 
-    uint4 xa[IPT], xb[IPT];
+    uint4 xa[IPT] = {}, xb[IPT] = {};
 #pragma unroll
     for (int k = 0; k < IPT; ++k) {
         const int item = item0 + k * blockDim.x;

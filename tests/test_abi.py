@@ -40,7 +40,8 @@ def test_header_declares_the_entry_points():
     assert names == {"rope_write_kv_packed", "rope_write_kv_continuous", "rope_write_kv_tree",
                      "paged_kv_delta_update", "paged_kv_delta_update_fused",
                      "dflash_prepare_delta_metadata", "dflash_gather_delta_rope",
-                     "rope_write_kv_slot_mapping", "rope_check_capacity",
+                     "rope_write_kv_slot_mapping", "rope_write_kv_continuous_qknorm",
+                     "rope_check_capacity",
                      "ropekv_status_string"}
 
 
@@ -192,3 +193,15 @@ def test_slot_mapping_rejects_bad_arguments(lib):
     assert _slotmap(lib, ptrs=[A, A, A, A, A, NUL, A, A, A, A]) == ERR["NULL"]
     assert _slotmap(lib, ptrs=[A, A, A, A, A, A, A, A, A, MIS]) == ERR["MISALIGNED"]
     assert _slotmap(lib, T=0, ptrs=[NUL] * 10) == OK
+
+
+def test_qknorm_rejects_bad_arguments(lib):
+    d = _dims()
+    f = lib.rope_write_kv_continuous_qknorm
+    assert f(A, A, A, A, A, A, A, -1.0, ctypes.byref(d), NUL) == ERR["SHAPE"]
+    assert f(A, A, A, A, A, A, A, float("nan"), ctypes.byref(d), NUL) == ERR["SHAPE"]
+    assert f(A, A, A, A, A, NUL, A, 1e-6, ctypes.byref(d), NUL) == ERR["NULL"]
+    assert f(A, A, A, A, A, A, MIS, 1e-6, ctypes.byref(d), NUL) == ERR["MISALIGNED"]
+    assert f(A, A, A, A, A, A, A, 1e-6, ctypes.byref(_dims(headDim=80, rotaryDim=80)),
+             NUL) == ERR["HEAD_DIM"]
+    assert f(NUL, NUL, NUL, NUL, NUL, NUL, NUL, 1e-6, ctypes.byref(_dims(batch=0)), NUL) == OK

@@ -19,6 +19,7 @@ SRC = os.path.join(ROOT, "oracle", "ropekv_oracle.c")
 HDR = os.path.join(ROOT, "oracle", "ropekv_oracle.h")
 PIN_TESTS = ["tests/test_oracle_rope.py", "tests/test_oracle_entries.py",
              "tests/test_oracle_dflash.py", "tests/test_oracle_slotmap.py",
+             "tests/test_oracle_qknorm.py", "tests/test_oracle_fp8.py",
              "tests/test_oracle_fp16.py"]
 
 MUTANTS = {
@@ -62,6 +63,17 @@ MUTANTS = {
     "slotmap_block_offset_swapped": ("int64_t block = slot / blockSize;\n        int64_t off = slot % blockSize;",
                                      "int64_t block = slot % blockSize;\n        int64_t off = slot / blockSize;"),
     "slotmap_negative_slot_written": ("if (slot < 0 || slot >= slots)", "if (slot >= slots)"),
+    "rmsnorm_mean_not_divided": ("double inv = 1.0 / sqrt(ss / D + eps);",
+                                 "double inv = 1.0 / sqrt(ss + eps);"),
+    "rmsnorm_eps_dropped": ("double inv = 1.0 / sqrt(ss / D + eps);",
+                            "double inv = 1.0 / sqrt(ss / D);"),
+    "qknorm_weights_swapped": ("norm_rope_head_f16(tok + (size_t)hq * D, qNormWeight,",
+                               "norm_rope_head_f16(tok + (size_t)hq * D, kNormWeight,"),
+    "e4m3_no_saturation": ("if (field > 15 || (field == 15 && q - 8.0 > 6.0))", "if (field > 16)"),
+    "e4m3_truncates": ("double q = nearbyint(ldexp(a, 3 - E));", "double q = floor(ldexp(a, 3 - E));"),
+    "e4m3_subnormal_scale": ("double k = nearbyint(ldexp(a, 9));", "double k = nearbyint(ldexp(a, 8));"),
+    "fp8_scale_not_inverted": ("kc[d] = ropekv_oracle_f64_to_e4m3(y[d] * (1.0 / (double)kScale));",
+                               "kc[d] = ropekv_oracle_f64_to_e4m3(y[d] * (double)kScale);"),
     "slotmap_stride_ignored": ("rope_head_f16(k + (size_t)t * kStride", "rope_head_f16(k + (size_t)t * Hkv * D"),
 }
 

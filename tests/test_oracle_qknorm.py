@@ -1,0 +1,83 @@
+"""Pins for the oracle's pre-RoPE QK RMS normalization.
+
+Reading of libmir-cuda execution.rs (qkv_postprocess: query_norm / key_norm
+weights, epsilon, then RoPE, then the KV store) and of "Dflash Runtime
+Kernels" (K deltas arrive "k_normed"): x_hat = x / sqrt(mean(x^2) + eps) * w
+per head, before the rotation. Pinned by closed forms (constant heads, unit
+RMS, scale invariance, a single weighted dim) and by reduction to the plain
+continuous call on inputs whose RMS is exactly 1.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+
+
+def _w(values):
+    return np.asarray(values, dtype=np.float64).astype(np.float16).view(np.uint16)
+
+
+def test_constant_head_normalizes_to_weight():
+    D = 64
+    for c in (3.0, -0.25, 1e-3):
+        y = oracle.rms_norm_f64(np.full(D, c), _w(np.ones(D)), 0.0)
+        assert np.allclose(y, np.sign(c), rtol=0, atol=1e-15)
+    # with eps: c / sqrt(c^2 + eps)
+    y = oracle.rms_norm_f64(np.full(D, 2.0), _w(np.ones(D)), 0.5)
+    assert np.allclose(y, 2.0 / math.sqrt(4.5), rtol=1e-15)
+
+
+def test_unit_rms_and_scale_invariance():
+    rng = np.random.Generator(np.random.PCG64(3))
+    for D in (64, 128, 256):
+        x = rng.standard_normal(D)
+        y = oracle.rms_norm_f64(x, _w(np.ones(D)), 0.0)
+        assert abs(math.sqrt(np.mean(y * y)) - 1.0) < 1e-14
+        y2 = oracle.rms_norm_f64(37.5 * x, _w(np.ones(D)), 0.0)
+        assert np.allclose(y, y2, rtol=1e-14, atol=0)
+
+
+def test_weight_scales_its_own_dim_only():
+    D = 128
+    x = np.linspace(-2, 2, D)
+    w = np.ones(D)
+    w[5] = 2.0
+    base = oracle.rms_norm_f64(x, _w(np.ones(D)), 1e-6)
+    y = oracle.rms_norm_f64(x, _w(w), 1e-6)
+    assert y[5] == 2 * base[5]
+    assert np.array_equal(np.delete(y, 5), np.delete(base, 5))
+
+
+@pytest.mark.parametrize("style", [oracle.NEOX, oracle.GPTJ])
+def test_unit_rms_inputs_reduce_to_the_plain_call(style):
+    """Heads of +-1 have RMS exactly 1: with unit weights and eps 0 the
+    normalized call must give the plain continuous call's bytes."""
+    rng = workloads.rng_for(8)
+    B, S, Hq, Hkv, D, r, cap = 2, 5, 4, 2, 64, 32, 16
+    signs = np.where(rng.random((B, S, Hq + 2 * Hkv, D)) < 0.5, -1.0, 1.0)
+    qkv = signs.astype(np.float16).view(np.uint16)
+    cs = workloads.cos_sin_table(1e4, cap, r)
+    end = np.array([7, 16], dtype=np.int32)
+    ones = _w(np.ones(D))
+    c1, q1 = workloads.sentinel_fill((B, 2, Hkv, cap, D)), workloads.sentinel_fill((B, S, Hq, D))
+    c2, q2 = workloads.sentinel_fill((B, 2, Hkv, cap, D)), workloads.sentinel_fill((B, S, Hq, D))
+    oracle.continuous(cs, end, qkv, c1, q1, Hq, Hkv, style)
+    oracle.continuous_qknorm(cs, end, qkv, c2, q2, ones, ones, 0.0, Hq, Hkv, style)
+    assert np.array_equal(c1, c2) and np.array_equal(q1, q2)
+
+
+def test_q_and_k_use_their_own_weights_and_v_is_copied():
+    B, S, Hq, Hkv, D, r, cap = 1, 1, 2, 1, 64, 64, 4
+    qkv = np.full((B, S, 4, D), 1.0).astype(np.float16).view(np.uint16)
+    cs = workloads.cos_sin_table(1e4, cap, r)     # position 0 is the identity row
+    end = np.array([1], dtype=np.int32)
+    cache = workloads.sentinel_fill((B, 2, Hkv, cap, D))
+    qo = workloads.sentinel_fill((B, S, Hq, D))
+    oracle.continuous_qknorm(cs, end, qkv, cache, qo, _w(np.full(D, 0.5)), _w(np.full(D, 4.0)),
+                             0.0, Hq, Hkv, oracle.NEOX)
+    assert np.all(qo.view(np.float16) == 0.5)
+    assert np.all(cache[0, 0, 0, 0].view(np.float16) == 4.0)
+    assert np.array_equal(cache[0, 1, 0, 0], qkv[0, 0, 3])

@@ -82,6 +82,9 @@ class ContiguousCase:
     pos_ids: Optional[np.ndarray] = None    # [B, S] int32
     cache_init: str = "sentinel"            # "sentinel" | "zero"
     name: str = ""
+    # pre-RoPE QK RMS norm (continuous call only): (q_weight [D], k_weight [D]
+    # uint16 FP16 bits, eps) or None
+    norm: Optional[tuple] = None
 
     @property
     def H(self) -> int:
@@ -109,6 +112,13 @@ class ContiguousCase:
         if self.mode == "packed":
             per_tok += self.Hkv * self.D * 2      # K also rotated in place in qkv
         return per_tok * self.tokens
+
+
+def norm_weights(seed: int, D: int, eps: float = 1e-6):
+    """RMS-norm weights for Q and K heads, 1 + 0.1 N(0,1) rounded to FP16, and eps."""
+    rng = rng_for(seed)
+    w = (1.0 + 0.1 * rng.standard_normal((2, D))).astype(np.float16).view(np.uint16)
+    return np.ascontiguousarray(w[0]), np.ascontiguousarray(w[1]), eps
 
 
 def random_tree_depths(rng: np.random.Generator, n: int, max_parent_depth: int = 5) -> np.ndarray:
@@ -496,7 +506,8 @@ CONFIG_NAMES = ("packed_tiny", "prefill", "decode", "tree", "paged")
 PROFILE_NAMES = ("decode_c1024", "paged_p8192")
 
 # Workloads of the next rows (built on the same kernels).
-NEXT_NAMES = ("paged_fused", "slotmap_prefill", "slotmap_decode")
+NEXT_NAMES = ("paged_fused", "slotmap_prefill", "slotmap_decode", "prefill_qknorm",
+              "decode_qknorm")
 
 
 def config(name: str):
@@ -534,6 +545,12 @@ def config(name: str):
     if name == "paged_p8192":
         return make_paged(16384, 128, 8, 128, 128, 64, 64, 8192, NEOX, 5e5, seed=4,
                           valid_rows=15565, name=name)
+    if name in ("prefill_qknorm", "decode_qknorm"):
+        # the prefill / decode workloads with pre-RoPE QK RMS norm fused in
+        case = config(name.split("_")[0])
+        case.norm = norm_weights(8, case.D)
+        case.name = name
+        return case
     if name == "slotmap_prefill":
         # the prefill above behind the sglang-style interface: 4 x 2048 tokens,
         # block size 64, 16384 blocks per cache, positions from start in [0, 4096]
