@@ -41,7 +41,8 @@ import workloads  # noqa: E402
 METRIC = "fused RoPE+KV-write tokens/s and effective HBM GB/s (% of GB300 peak)"
 HEADLINE = "prefill"
 EXTRA = ("decode", "tree", "paged", "packed_tiny", "paged_fused", "paged_fused_3launch",
-         "slotmap_prefill", "slotmap_decode", "prefill_qknorm", "decode_qknorm")
+         "slotmap_prefill", "slotmap_decode", "prefill_qknorm", "decode_qknorm", "prefill_fp8",
+         "decode_fp8")
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 
@@ -65,6 +66,8 @@ DESCR = {
     "slotmap_decode": "256 one-token decodes behind the sglang-style interface",
     "prefill_qknorm": "the prefill with pre-RoPE QK RMS norm fused in (weights [128], eps 1e-6)",
     "decode_qknorm": "the decode with pre-RoPE QK RMS norm fused in (weights [128], eps 1e-6)",
+    "prefill_fp8": "the prefill with an E4M3 KV cache (k_scale 0.05, v_scale 0.04)",
+    "decode_fp8": "the decode with an E4M3 KV cache (k_scale 0.05, v_scale 0.04)",
     "decode_c1024": "decode as above with cache capacity 1024 (profiler-sized twin)",
     "paged_p8192": "paged as above with 64 pages/seq and 8192 pages per plane (profiler-sized twin)",
 }
@@ -245,8 +248,15 @@ class DeviceWorkload:
             self.norm = None
             if c.norm is not None:
                 self.norm = (t(c.norm[0]), t(c.norm[1]), float(c.norm[2]))
-            self.cache = (t(c.new_cache()) if c.cache_init == "zero"
-                          else self._sentinel((c.B, 2, c.Hkv, c.cap, c.D)))
+            self.fp8 = None
+            if c.fp8_scales is not None:
+                self.fp8 = tuple(torch.tensor([v], dtype=torch.float32, device=device)
+                                 for v in c.fp8_scales)
+                self.cache = torch.full((c.B, 2, c.Hkv, c.cap, c.D), workloads.SENTINEL8,
+                                        dtype=torch.uint8, device=device)
+            else:
+                self.cache = (t(c.new_cache()) if c.cache_init == "zero"
+                              else self._sentinel((c.B, 2, c.Hkv, c.cap, c.D)))
             qkv_base = t(c.qkv)
             for k in range(self.ring):
                 end, pos = workloads.step_variant(c, k)
@@ -316,6 +326,10 @@ class DeviceWorkload:
         elif c.mode == "tree":
             rk.rope_write_kv_tree(self.cos_sin, s["end"], s["pos"], s["qkv"], self.cache,
                                   s["qout"], c.Hq, c.Hkv, c.style, stream=stream)
+        elif self.fp8 is not None:
+            rk.rope_write_kv_continuous_fp8(self.cos_sin, s["end"], s["qkv"], self.cache,
+                                            s["qout"], self.fp8[0], self.fp8[1], c.Hq, c.Hkv,
+                                            c.style, stream=stream)
         elif self.norm is not None:
             qw, kw, eps = self.norm
             rk.rope_write_kv_continuous_qknorm(self.cos_sin, s["end"], s["qkv"], self.cache,
@@ -590,7 +604,8 @@ def main(argv=None):
     achieved = wl.bytes / launch_s / 1e9
     clocks = sampler.summary(t0, t1) if sampler else None
     e2e = e2e_contiguous(wl, args.e2e_steps) \
-        if not (wl.paged or wl.fused or wl.slotmap) else None
+        if not (wl.paged or wl.fused or wl.slotmap or wl.case.norm is not None
+                or wl.case.fp8_scales is not None) else None
     tokens, bytes_step, ring = wl.tokens, wl.bytes, wl.ring
     kernel = _kernel_name(wl)
     del wl
@@ -673,7 +688,8 @@ def _kernel_name(wl) -> str:
     if wl.paged:
         return f"paged_delta_kernel<D={c.D}, {'NeoX' if c.style == 0 else 'GPT-J'}>"
     return (f"rope_kv_token_kernel<D={c.D}, {'NeoX' if c.style == 0 else 'GPT-J'}, "
-            f"{c.mode}{', qk-norm' if c.norm is not None else ''}>")
+            f"{c.mode}{', qk-norm' if c.norm is not None else ''}"
+            f"{', e4m3 cache' if c.fp8_scales is not None else ''}>")
 
 
 if __name__ == "__main__":

@@ -140,6 +140,22 @@ ROPEKV_API int rope_write_kv_continuous_qknorm(const float* cosSin,
                                                const ropekv_dims* dims, void* stream);
 
 /*
+ * rope_write_kv_continuous with an FP8 cache ([RC] kernel Stage 3.3: rotated K
+ * and V are multiplied by 1/k_scale and 1/v_scale and stored in the cache's FP8
+ * type). Cache elements are OCP E4M3 ("e4m3fn") bytes: plane 0 =
+ * e4m3(rotated K * (1 / *kScale)), plane 1 = e4m3(V * (1 / *vScale)), rounded to
+ * nearest even from FP32 and saturated to +-448. Rotated Q goes to qOut in FP16.
+ *   kvCache8        [B, 2, Hkv, kvCapacity, headDim] uint8 (E4M3), written at the slots.
+ *   kScale, vScale  one FP32 each, device memory, read by the kernel (> 0).
+ * Everything else as rope_write_kv_continuous.
+ */
+ROPEKV_API int rope_write_kv_continuous_fp8(const float* cosSin, const int32_t* kvCacheEndLens,
+                                            const uint16_t* qkv, uint8_t* kvCache8,
+                                            uint16_t* qOut, const float* kScale,
+                                            const float* vScale, const ropekv_dims* dims,
+                                            void* stream);
+
+/*
  * [ARW] launchApplyRopeWriteKVTreeDecoding: tree attention for speculative
  * decoding. As the continuous call, except that the RoPE position of token
  * (b, s) is tokenPosIds[b, s] ("position of token within sequence"); the cache

@@ -17,6 +17,7 @@ from ._binding import (  # noqa: F401
     paged_kv_delta_update_fused,
     rope_check_capacity,
     rope_write_kv_continuous,
+    rope_write_kv_continuous_fp8,
     rope_write_kv_continuous_qknorm,
     rope_write_kv_packed,
     rope_write_kv_slot_mapping,
@@ -27,6 +28,7 @@ from ._binding import (  # noqa: F401
 __all__ = [
     "NEOX", "GPTJ", "RopeKVError", "load_library", "library_path",
     "rope_write_kv_packed", "rope_write_kv_continuous", "rope_write_kv_continuous_qknorm",
+    "rope_write_kv_continuous_fp8",
     "rope_write_kv_tree",
     "paged_kv_delta_update", "paged_kv_delta_update_fused", "dflash_prepare_delta_metadata",
     "dflash_gather_delta_rope", "rope_write_kv_slot_mapping", "rope_check_capacity",

@@ -60,6 +60,7 @@ def load_library():
     lib.rope_write_kv_continuous.argtypes = [P, P, P, P, P, D, P]
     lib.rope_write_kv_tree.argtypes = [P, P, P, P, P, P, D, P]
     lib.rope_write_kv_continuous_qknorm.argtypes = [P, P, P, P, P, P, P, ctypes.c_float, D, P]
+    lib.rope_write_kv_continuous_fp8.argtypes = [P, P, P, P, P, P, P, D, P]
     lib.paged_kv_delta_update.argtypes = [P] * 7 + [I32] * 9 + [P]
     lib.paged_kv_delta_update_fused.argtypes = [P] * 6 + [I32] + [P] * 2 + [I32] * 10 + [P]
     lib.dflash_prepare_delta_metadata.argtypes = [P, P, I32, P, P, I32, P]
@@ -71,7 +72,7 @@ def load_library():
     lib.ropekv_status_string.argtypes = [ctypes.c_int]
     lib.ropekv_status_string.restype = ctypes.c_char_p
     for fn in ("rope_write_kv_packed", "rope_write_kv_continuous", "rope_write_kv_tree",
-               "rope_write_kv_continuous_qknorm",
+               "rope_write_kv_continuous_qknorm", "rope_write_kv_continuous_fp8",
                "paged_kv_delta_update", "paged_kv_delta_update_fused",
                "dflash_prepare_delta_metadata", "dflash_gather_delta_rope",
                "rope_write_kv_slot_mapping", "rope_check_capacity"):
@@ -212,6 +213,31 @@ def rope_write_kv_continuous_qknorm(cos_sin: torch.Tensor, kv_cache_end_lens: to
         _dev_ptr(k_norm_weight, "k_norm_weight", _F16, dev), float(eps), ctypes.byref(dims),
         _stream_handle(stream, dev))
     _check_rc("rope_write_kv_continuous_qknorm", rc)
+
+
+_U8 = (torch.uint8, torch.float8_e4m3fn) if hasattr(torch, "float8_e4m3fn") else (torch.uint8,)
+
+
+def rope_write_kv_continuous_fp8(cos_sin: torch.Tensor, kv_cache_end_lens: torch.Tensor,
+                                 qkv: torch.Tensor, kv_cache: torch.Tensor, q_out: torch.Tensor,
+                                 k_scale: torch.Tensor, v_scale: torch.Tensor,
+                                 num_q_heads: int, num_kv_heads: int, style: int = NEOX,
+                                 stream: Optional[torch.cuda.Stream] = None) -> None:
+    """rope_write_kv_continuous with an E4M3 cache [B, 2, Hkv, cap, D] (uint8 or
+    float8_e4m3fn) and per-tensor scales (one-element float32 device tensors)."""
+    dims = _contiguous_dims(cos_sin, qkv, kv_cache, num_q_heads, num_kv_heads, style)
+    B, S, _, D = qkv.shape
+    if tuple(kv_cache_end_lens.shape) != (B,) or tuple(q_out.shape) != (B, S, num_q_heads, D) \
+            or k_scale.numel() != 1 or v_scale.numel() != 1:
+        raise ValueError("kv_cache_end_lens [B], q_out [B,S,Hq,D], one-element scales expected")
+    dev = qkv.device
+    rc = load_library().rope_write_kv_continuous_fp8(
+        _dev_ptr(cos_sin, "cos_sin", _F32, dev),
+        _dev_ptr(kv_cache_end_lens, "kv_cache_end_lens", _I32, dev),
+        _dev_ptr(qkv, "qkv", _F16, dev), _dev_ptr(kv_cache, "kv_cache", _U8, dev),
+        _dev_ptr(q_out, "q_out", _F16, dev), _dev_ptr(k_scale, "k_scale", _F32, dev),
+        _dev_ptr(v_scale, "v_scale", _F32, dev), ctypes.byref(dims), _stream_handle(stream, dev))
+    _check_rc("rope_write_kv_continuous_fp8", rc)
 
 
 def rope_write_kv_tree(cos_sin: torch.Tensor, kv_cache_end_lens: torch.Tensor,

@@ -78,6 +78,9 @@ void launch_token(const TokenArgs& a, long long tokens, const Shape& sh, cudaStr
     if (MODE == ropekv::kContinuous && a.qNormW != nullptr)
         ropekv::rope_kv_token_kernel<D, STYLE, MODE, IPT, kPolicy, true>
             <<<grid, sh.threads, 0, st>>>(a);
+    else if (MODE == ropekv::kContinuous && a.cache8 != nullptr)
+        ropekv::rope_kv_token_kernel<D, STYLE, MODE, IPT, kPolicy, false, true>
+            <<<grid, sh.threads, 0, st>>>(a);
     else
         ropekv::rope_kv_token_kernel<D, STYLE, MODE, IPT, kPolicy, false>
             <<<grid, sh.threads, 0, st>>>(a);
@@ -314,6 +317,33 @@ int rope_write_kv_continuous_qknorm(const float* cosSin, const int32_t* kvCacheE
     a.qNormW = qNormWeight;
     a.kNormW = kNormWeight;
     a.eps = eps;
+    return launch_contiguous(a, dims, tokens, ropekv::kContinuous, (cudaStream_t)stream);
+}
+
+int rope_write_kv_continuous_fp8(const float* cosSin, const int32_t* kvCacheEndLens,
+                                 const uint16_t* qkv, uint8_t* kvCache8, uint16_t* qOut,
+                                 const float* kScale, const float* vScale,
+                                 const ropekv_dims* dims, void* stream)
+{
+    long long tokens = 0;
+    int rc = check_dims(dims, &tokens);
+    if (rc != ROPEKV_OK)
+        return rc;
+    if (tokens == 0)
+        return ROPEKV_OK;
+    if (!cosSin || !kvCacheEndLens || !qkv || !kvCache8 || !qOut || !kScale || !vScale)
+        return ROPEKV_ERR_NULL_POINTER;
+    if (!aligned16(cosSin) || !aligned16(kvCacheEndLens) || !aligned16(qkv) ||
+        !aligned16(kvCache8) || !aligned16(qOut) || !aligned16(kScale) || !aligned16(vScale))
+        return ROPEKV_ERR_MISALIGNED;
+    TokenArgs a = token_args(dims);
+    a.cosSin = cosSin;
+    a.endLens = kvCacheEndLens;
+    a.qkv = qkv;
+    a.cache8 = kvCache8;
+    a.qOut = qOut;
+    a.kScale = kScale;
+    a.vScale = vScale;
     return launch_contiguous(a, dims, tokens, ropekv::kContinuous, (cudaStream_t)stream);
 }
 

@@ -30,6 +30,7 @@
 #pragma once
 
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <stdint.h>
 
 namespace ropekv {
@@ -49,6 +50,9 @@ struct TokenArgs {
     const uint16_t* qNormW;    // [D] FP16 RMS-norm weight of Q heads (normalized call)
     const uint16_t* kNormW;    // [D] FP16 RMS-norm weight of K heads (normalized call)
     float eps;                 // RMS-norm epsilon (normalized call)
+    uint8_t* cache8;           // [B, 2, Hkv, cap, D] E4M3 cache (FP8 call; replaces cache)
+    const float* kScale;       // K scale of the FP8 cache (device scalar)
+    const float* vScale;       // V scale of the FP8 cache (device scalar)
     int32_t S, Hq, Hkv, r, cap, csBatch, csSeq;
     int32_t itemsPerToken;     // (Hq + 2 Hkv) * D / 16
     int32_t ctasPerToken;      // CTAs sharing one token's items
@@ -305,6 +309,29 @@ __device__ __forceinline__ uint4 pack8(const float f[8])
     return v;
 }
 
+// 8 FP32 values -> 8 E4M3 bytes: round to nearest even, saturating to the
+// largest finite value (CUDA's satfinite conversion).
+__device__ __forceinline__ uint2 pack8_e4m3(const float f[8])
+{
+    const uint32_t p0 = __nv_cvt_float2_to_fp8x2(make_float2(f[0], f[1]), __NV_SATFINITE, __NV_E4M3);
+    const uint32_t p1 = __nv_cvt_float2_to_fp8x2(make_float2(f[2], f[3]), __NV_SATFINITE, __NV_E4M3);
+    const uint32_t p2 = __nv_cvt_float2_to_fp8x2(make_float2(f[4], f[5]), __NV_SATFINITE, __NV_E4M3);
+    const uint32_t p3 = __nv_cvt_float2_to_fp8x2(make_float2(f[6], f[7]), __NV_SATFINITE, __NV_E4M3);
+    return make_uint2(p0 | (p1 << 16), p2 | (p3 << 16));
+}
+
+template <int POL>
+__device__ __forceinline__ void store_v8(uint8_t* p, const uint2& v, const L2Policies& pol)
+{
+    if (POL & kStreamHint) {
+        asm volatile("st.global.L2::cache_hint.v2.u32 [%0], {%1,%2}, %3;"
+                     :: "l"(p), "r"(v.x), "r"(v.y), "l"(pol.stream)
+                     : "memory");
+        return;
+    }
+    *reinterpret_cast<uint2*>(p) = v;
+}
+
 // The rotation of rotate_item on FP32 values (fa, fb: the item's two vectors).
 template <int STYLE>
 __device__ __forceinline__ void rotate_item_f32(float fa[8], float fb[8], const float c[8],
@@ -354,7 +381,11 @@ __device__ __forceinline__ void rotate_item(uint4& va, uint4& vb, const float c[
 // rotated, then rounded once. A head's D/16 items sit in D/16 consecutive lanes
 // of one warp (items are head-major and blocks are whole warps), so the sum of
 // squares is one xor-shuffle reduction over those lanes.
-template <int D, int STYLE, int MODE, int IPT, int POL, bool NORM = false>
+//
+// FP8 (continuous only): the cache is E4M3; K (after the rotation, in FP32)
+// and V are multiplied by 1/kScale and 1/vScale and stored as 8-byte vectors
+// ("rope_cache.py", Stage 3.3). Q is written in FP16 as usual.
+template <int D, int STYLE, int MODE, int IPT, int POL, bool NORM = false, bool FP8 = false>
 __global__ void __launch_bounds__(256) rope_kv_token_kernel(const TokenArgs a)
 {
     constexpr int kItemsPerHead = D / 16;
@@ -453,12 +484,38 @@ __global__ void __launch_bounds__(256) rope_kv_token_kernel(const TokenArgs a)
     }
 
     // 4. rotate and store
+    float invK = 1.0f, invV = 1.0f;
+    if (FP8) {
+        invK = 1.0f / __ldg(a.kScale);
+        invV = 1.0f / __ldg(a.vScale);
+    }
 #pragma unroll
     for (int k = 0; k < IPT; ++k) {
         const int item = item0 + k * blockDim.x;
         if (item >= a.itemsPerToken)
             continue;
         const int head = item / kItemsPerHead;
+        if (FP8 && head >= a.Hq) {
+            // K or V into the E4M3 cache: FP32 value times the inverse scale
+            float fa[8], fb[8];
+            unpack8(xa[k], fa);
+            unpack8(xb[k], fb);
+            const bool isK = head < a.Hq + a.Hkv;
+            if (isK && rotItem)
+                rotate_item_f32<STYLE>(fa, fb, c, sn);
+            const float inv = isK ? invK : invV;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                fa[j] *= inv;
+                fb[j] *= inv;
+            }
+            const int plane = isK ? 0 : 1;
+            const int hk = isK ? head - a.Hq : head - a.Hq - a.Hkv;
+            uint8_t* dst = a.cache8 + ((((size_t)b * 2 + plane) * a.Hkv + hk) * a.cap + slot) * D;
+            store_v8<POL>(dst + 8 * va, pack8_e4m3(fa), pol);
+            store_v8<POL>(dst + 8 * vb, pack8_e4m3(fb), pol);
+            continue;
+        }
         uint16_t* dst;
         if (head < a.Hq + a.Hkv) {
             if (!NORM && rotItem)

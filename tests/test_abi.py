@@ -41,6 +41,7 @@ def test_header_declares_the_entry_points():
                      "paged_kv_delta_update", "paged_kv_delta_update_fused",
                      "dflash_prepare_delta_metadata", "dflash_gather_delta_rope",
                      "rope_write_kv_slot_mapping", "rope_write_kv_continuous_qknorm",
+                     "rope_write_kv_continuous_fp8",
                      "rope_check_capacity",
                      "ropekv_status_string"}
 
@@ -205,3 +206,12 @@ def test_qknorm_rejects_bad_arguments(lib):
     assert f(A, A, A, A, A, A, A, 1e-6, ctypes.byref(_dims(headDim=80, rotaryDim=80)),
              NUL) == ERR["HEAD_DIM"]
     assert f(NUL, NUL, NUL, NUL, NUL, NUL, NUL, 1e-6, ctypes.byref(_dims(batch=0)), NUL) == OK
+
+
+def test_fp8_rejects_bad_arguments(lib):
+    d = _dims()
+    f = lib.rope_write_kv_continuous_fp8
+    assert f(A, A, A, A, A, NUL, A, ctypes.byref(d), NUL) == ERR["NULL"]
+    assert f(A, A, A, MIS, A, A, A, ctypes.byref(d), NUL) == ERR["MISALIGNED"]
+    assert f(A, A, A, A, A, A, A, ctypes.byref(_dims(rotaryDim=40)), NUL) == ERR["ROTARY_DIM"]
+    assert f(NUL, NUL, NUL, NUL, NUL, NUL, NUL, ctypes.byref(_dims(seqLen=0)), NUL) == OK

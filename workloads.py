@@ -25,6 +25,9 @@ GPTJ = 1
 # no finite input or rotated value can produce, so any byte the call did not
 # write is recognisable afterwards.
 SENTINEL = 0x7E5A
+# The same for E4M3 caches: 0x7F is NaN there, and the saturating store never
+# produces NaN from finite values.
+SENTINEL8 = 0x7F
 
 
 def rng_for(seed: int) -> np.random.Generator:
@@ -85,6 +88,8 @@ class ContiguousCase:
     # pre-RoPE QK RMS norm (continuous call only): (q_weight [D], k_weight [D]
     # uint16 FP16 bits, eps) or None
     norm: Optional[tuple] = None
+    # FP8 (E4M3) cache (continuous call only): (k_scale, v_scale) or None
+    fp8_scales: Optional[tuple] = None
 
     @property
     def H(self) -> int:
@@ -103,12 +108,17 @@ class ContiguousCase:
     def new_qout(self) -> np.ndarray:
         return sentinel_fill((self.B, self.S, self.Hq, self.D))
 
+    def new_cache8(self) -> np.ndarray:
+        """E4M3 cache filled with 0x7F, a NaN no saturating conversion produces."""
+        return np.full((self.B, 2, self.Hkv, self.cap, self.D), SENTINEL8, dtype=np.uint8)
+
     def algorithmic_bytes(self) -> int:
         """QKV read + cos/sin read (one row per token) + Q, K, V written."""
+        kv_elem = 1 if self.fp8_scales is not None else 2
         per_tok = (self.H * self.D * 2            # packed QKV row read
                    + self.r * 4                   # cos/sin row read
                    + self.Hq * self.D * 2         # Q written (qOut, or in place)
-                   + 2 * self.Hkv * self.D * 2)   # K and V cache rows written
+                   + 2 * self.Hkv * self.D * kv_elem)  # K and V cache rows written
         if self.mode == "packed":
             per_tok += self.Hkv * self.D * 2      # K also rotated in place in qkv
         return per_tok * self.tokens
@@ -507,7 +517,7 @@ PROFILE_NAMES = ("decode_c1024", "paged_p8192")
 
 # Workloads of the next rows (built on the same kernels).
 NEXT_NAMES = ("paged_fused", "slotmap_prefill", "slotmap_decode", "prefill_qknorm",
-              "decode_qknorm")
+              "decode_qknorm", "prefill_fp8", "decode_fp8")
 
 
 def config(name: str):
@@ -549,6 +559,12 @@ def config(name: str):
         # the prefill / decode workloads with pre-RoPE QK RMS norm fused in
         case = config(name.split("_")[0])
         case.norm = norm_weights(8, case.D)
+        case.name = name
+        return case
+    if name in ("prefill_fp8", "decode_fp8"):
+        # the prefill / decode workloads with an E4M3 cache, per-tensor scales
+        case = config(name.split("_")[0])
+        case.fp8_scales = (0.05, 0.04)
         case.name = name
         return case
     if name == "slotmap_prefill":
