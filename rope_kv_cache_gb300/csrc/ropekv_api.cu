@@ -49,11 +49,16 @@ struct Shape {
     int ctasPerUnit;
 };
 
-Shape pick_shape(int items, long long units)
+Shape pick_shape(int items, long long units, bool heavy = false)
 {
     Shape sh;
     int perCta;
-    if (units >= 1024) {
+    if (heavy) {
+        // the QK-normalized call does ~3x the arithmetic per byte: more items
+        // per thread keep more loads in flight while it computes (measured)
+        sh.ipt = units >= 1024 ? 4 : 1;
+        perCta = units >= 1024 ? 128 : 64;
+    } else if (units >= 1024) {
         sh.ipt = 2;
         perCta = 128;
     } else {
@@ -75,24 +80,36 @@ template <int D, int STYLE, int MODE, int IPT>
 void launch_token(const TokenArgs& a, long long tokens, const Shape& sh, cudaStream_t st)
 {
     const unsigned grid = (unsigned)(tokens * sh.ctasPerUnit);
-    if (MODE == ropekv::kContinuous && a.qNormW != nullptr)
-        ropekv::rope_kv_token_kernel<D, STYLE, MODE, IPT, kPolicy, true>
-            <<<grid, sh.threads, 0, st>>>(a);
-    else if (MODE == ropekv::kContinuous && a.cache8 != nullptr)
-        ropekv::rope_kv_token_kernel<D, STYLE, MODE, IPT, kPolicy, false, true>
-            <<<grid, sh.threads, 0, st>>>(a);
-    else
-        ropekv::rope_kv_token_kernel<D, STYLE, MODE, IPT, kPolicy, false>
-            <<<grid, sh.threads, 0, st>>>(a);
+    if constexpr (MODE == ropekv::kContinuous) {
+        if (a.qNormW != nullptr) {
+            ropekv::rope_kv_token_kernel<D, STYLE, MODE, IPT, kPolicy, true>
+                <<<grid, sh.threads, 0, st>>>(a);
+            return;
+        }
+        if (a.cache8 != nullptr) {
+            ropekv::rope_kv_token_kernel<D, STYLE, MODE, IPT, kPolicy, false, true>
+                <<<grid, sh.threads, 0, st>>>(a);
+            return;
+        }
+    }
+    ropekv::rope_kv_token_kernel<D, STYLE, MODE, IPT, kPolicy, false>
+        <<<grid, sh.threads, 0, st>>>(a);
 }
 
 template <int D, int STYLE, int MODE>
 void dispatch_ipt(const TokenArgs& a, long long tokens, const Shape& sh, cudaStream_t st)
 {
-    if (sh.ipt == 2)
+    if (sh.ipt == 2) {
         launch_token<D, STYLE, MODE, 2>(a, tokens, sh, st);
-    else
+    } else if (sh.ipt == 4) {
+        if constexpr (MODE == ropekv::kContinuous) {
+            const unsigned grid = (unsigned)(tokens * sh.ctasPerUnit);
+            ropekv::rope_kv_token_kernel<D, STYLE, MODE, 4, kPolicy, true>
+                <<<grid, sh.threads, 0, st>>>(a);
+        }
+    } else {
         launch_token<D, STYLE, MODE, 1>(a, tokens, sh, st);
+    }
 }
 
 template <int D, int MODE>
@@ -220,7 +237,7 @@ TokenArgs token_args(const ropekv_dims* d)
 int launch_contiguous(TokenArgs a, const ropekv_dims* d, long long tokens, int mode,
                       cudaStream_t st)
 {
-    const Shape sh = pick_shape(a.itemsPerToken, tokens);
+    const Shape sh = pick_shape(a.itemsPerToken, tokens, a.qNormW != nullptr);
     if (tokens * sh.ctasPerUnit > 0x7FFFFFFFLL)
         return ROPEKV_ERR_SHAPE;
     a.ctasPerToken = sh.ctasPerUnit;

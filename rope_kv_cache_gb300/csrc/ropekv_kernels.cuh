@@ -443,12 +443,12 @@ __global__ void __launch_bounds__(256) rope_kv_token_kernel(const TokenArgs a)
     }
 
     if (NORM) {
-        // weights of this lane's 16 dims, for Q heads and for K heads
-        float wq[16], wk[16];
-        unpack8(__ldg(reinterpret_cast<const uint4*>(a.qNormW + 8 * va)), wq);
-        unpack8(__ldg(reinterpret_cast<const uint4*>(a.qNormW + 8 * vb)), wq + 8);
-        unpack8(__ldg(reinterpret_cast<const uint4*>(a.kNormW + 8 * va)), wk);
-        unpack8(__ldg(reinterpret_cast<const uint4*>(a.kNormW + 8 * vb)), wk + 8);
+        // weights of this lane's 16 dims, for Q heads and for K heads (kept
+        // packed, unpacked where used)
+        const uint4 wqa = __ldg(reinterpret_cast<const uint4*>(a.qNormW + 8 * va));
+        const uint4 wqb = __ldg(reinterpret_cast<const uint4*>(a.qNormW + 8 * vb));
+        const uint4 wka = __ldg(reinterpret_cast<const uint4*>(a.kNormW + 8 * va));
+        const uint4 wkb = __ldg(reinterpret_cast<const uint4*>(a.kNormW + 8 * vb));
 #pragma unroll
         for (int k = 0; k < IPT; ++k) {
             const int item = item0 + k * blockDim.x;
@@ -470,12 +470,16 @@ __global__ void __launch_bounds__(256) rope_kv_token_kernel(const TokenArgs a)
             if (!qk)
                 continue;
             const float inv = rsqrtf(ss * (1.0f / D) + a.eps);
-            const float* w = head < a.Hq ? wq : wk;
+            const bool isQ = head < a.Hq;
+            float w[8];
+            unpack8(isQ ? wqa : wka, w);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
+            for (int j = 0; j < 8; ++j)
                 fa[j] = fa[j] * inv * w[j];
-                fb[j] = fb[j] * inv * w[8 + j];
-            }
+            unpack8(isQ ? wqb : wkb, w);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                fb[j] = fb[j] * inv * w[j];
             if (rotItem)
                 rotate_item_f32<STYLE>(fa, fb, c, sn);
             xa[k] = pack8(fa);
