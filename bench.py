@@ -70,6 +70,8 @@ DESCR = {
     "decode_fp8": "the decode with an E4M3 KV cache (k_scale 0.05, v_scale 0.04)",
     "decode_c1024": "decode as above with cache capacity 1024 (profiler-sized twin)",
     "paged_p8192": "paged as above with 64 pages/seq and 8192 pages per plane (profiler-sized twin)",
+    "paged_fused_p8192": "paged_fused with 64 pages/seq and 8192 pages per plane (profiler-sized twin)",
+    "slotmap_prefill_b4096": "slotmap_prefill with 4096 blocks per cache (profiler-sized twin)",
 }
 
 

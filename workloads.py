@@ -513,7 +513,7 @@ CONFIG_NAMES = ("packed_tiny", "prefill", "decode", "tree", "paged")
 # Smaller-footprint twins of two workloads for profiler captures: the same
 # tokens / rows per launch, a smaller cache (decode: capacity 1024) or pool
 # (paged: 64 logical pages per sequence, 8192 pages per plane, positions < 4096).
-PROFILE_NAMES = ("decode_c1024", "paged_p8192")
+PROFILE_NAMES = ("decode_c1024", "paged_p8192", "paged_fused_p8192", "slotmap_prefill_b4096")
 
 # Workloads of the next rows (built on the same kernels).
 NEXT_NAMES = ("paged_fused", "slotmap_prefill", "slotmap_decode", "prefill_qknorm",
@@ -576,6 +576,12 @@ def config(name: str):
         # 256 one-token sequences at positions in [0, 8191], one slot each
         return make_slotmap([1] * 256, 32, 8, 128, 128, NEOX, 5e5, seed=7, block_size=64,
                             num_blocks=16384, start_range=(0, 8191), cs_rows=8192, name=name)
+    if name == "paged_fused_p8192":
+        return make_paged_fused(128, 128, 8, 128, 128, 64, 64, 8192, NEOX, 5e5, seed=5,
+                                name=name)
+    if name == "slotmap_prefill_b4096":
+        return make_slotmap([2048] * 4, 32, 8, 128, 128, NEOX, 5e5, seed=6, block_size=64,
+                            num_blocks=4096, start_range=(0, 4096), cs_rows=8192, name=name)
     if name == "paged_fused":
         # the DFlash step in one launch: B=128 sequences x deltaWidth 128 rows
         # (16384 rows), delta lengths uniform in [1, 128], Hkv=8, D=r=128,
