@@ -124,7 +124,25 @@ struct GatherArgs {
 //                them bypassing L1 and mark loads and stores evict-first in L2.
 //   kTableKeep:  cos/sin rows are reused by every call: mark them evict-last
 //                in L2 so the streaming traffic does not push them out.
-enum Policy : int { kPdl = 1, kStreamHint = 2, kTableKeep = 4 };
+//   kPrefetch:   (with kPdl) before waiting for the previous grid, warm L2 with
+//                the thread's input vectors and the cos/sin row of the token's
+//                speculatively read position. Only L2 prefetches and
+//                L1-bypassing loads happen before the wait, so nothing stale can
+//                be consumed afterwards (L2 is the point of coherence), and a
+//                wrong speculative position only wastes one prefetch.
+enum Policy : int { kPdl = 1, kStreamHint = 2, kTableKeep = 4, kPrefetch = 8 };
+
+__device__ __forceinline__ void prefetch_l2(const void* p)
+{
+    asm volatile("prefetch.global.L2 [%0];" :: "l"(p));
+}
+
+__device__ __forceinline__ int load_int_l2(const int32_t* p)
+{
+    int v;
+    asm volatile("ld.global.cg.s32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
 
 struct L2Policies {
     uint64_t stream;
@@ -389,8 +407,6 @@ template <int D, int STYLE, int MODE, int IPT, int POL, bool NORM = false, bool 
 __global__ void __launch_bounds__(256) rope_kv_token_kernel(const TokenArgs a)
 {
     constexpr int kItemsPerHead = D / 16;
-    grid_dependency_sync<POL>();
-    const L2Policies pol = make_policies<POL>();
     const int tok = blockIdx.x / a.ctasPerToken;
     const int part = blockIdx.x - tok * a.ctasPerToken;
     const int b = tok / a.S;
@@ -401,9 +417,30 @@ __global__ void __launch_bounds__(256) rope_kv_token_kernel(const TokenArgs a)
 
     int va, vb;
     item_vectors<D>(i, a.r, va, vb);
+    const uint16_t* tokIn = a.qkv + (size_t)tok * H * D;
+
+    if ((POL & kPdl) && (POL & kPrefetch)) {
+#pragma unroll
+        for (int k = 0; k < IPT; ++k) {
+            const int item = item0 + k * blockDim.x;
+            if (item < a.itemsPerToken) {
+                const uint16_t* p = tokIn + (size_t)(item / kItemsPerHead) * D;
+                prefetch_l2(p + 8 * va);
+                prefetch_l2(p + 8 * vb);
+            }
+        }
+        if (MODE != kPacked && i < (a.r >> 4) && a.csSeq > 0) {
+            int pos = (MODE == kTree) ? load_int_l2(a.posIds + tok)
+                                      : load_int_l2(a.endLens + b) - a.S + s;
+            pos = min(max(pos, 0), a.csSeq - 1);
+            const int bc = (a.csBatch == 1) ? 0 : b;
+            prefetch_l2(a.cosSin + ((size_t)bc * a.csSeq + pos) * a.r + (STYLE == kNeox ? 8 : 4) * i);
+        }
+    }
+    grid_dependency_sync<POL>();
+    const L2Policies pol = make_policies<POL>();
 
     // 1. this thread's QKV vectors (independent of the position chain)
-    const uint16_t* tokIn = a.qkv + (size_t)tok * H * D;
     uint4 xa[IPT] = {}, xb[IPT] = {};
 #pragma unroll
     for (int k = 0; k < IPT; ++k) {
@@ -668,8 +705,6 @@ template <int D, int STYLE, int IPT, int POL>
 __global__ void __launch_bounds__(256) rope_kv_slotmap_kernel(const SlotMapArgs a)
 {
     constexpr int kItemsPerHead = D / 16;
-    grid_dependency_sync<POL>();
-    const L2Policies pol = make_policies<POL>();
     const int tok = blockIdx.x / a.ctasPerToken;
     const int part = blockIdx.x - tok * a.ctasPerToken;
     const int i = threadIdx.x % kItemsPerHead;
@@ -678,6 +713,31 @@ __global__ void __launch_bounds__(256) rope_kv_slotmap_kernel(const SlotMapArgs 
 
     int va, vb;
     item_vectors<D>(i, a.r, va, vb);
+
+    if ((POL & kPdl) && (POL & kPrefetch)) {
+        // L2 prefetches only (see kPrefetch): inputs, then the cos/sin row of
+        // the speculatively read position, clamped into the table
+#pragma unroll
+        for (int k = 0; k < IPT; ++k) {
+            const int item = item0 + k * blockDim.x;
+            if (item < a.itemsPerToken) {
+                const int head = item / kItemsPerHead;
+                const uint16_t* p = head < a.Hq ? a.q + tok * a.qStride + (size_t)head * D
+                                  : head < qkHeads ? a.k + tok * a.kStride + (size_t)(head - a.Hq) * D
+                                  : a.v + tok * a.vStride + (size_t)(head - qkHeads) * D;
+                prefetch_l2(p + 8 * va);
+                prefetch_l2(p + 8 * vb);
+            }
+        }
+        if (i < (a.r >> 4) && a.csRows > 0) {
+            int64_t pos;
+            asm volatile("ld.global.cg.s64 %0, [%1];" : "=l"(pos) : "l"(a.positions + tok));
+            pos = pos < 0 ? 0 : (pos >= a.csRows ? a.csRows - 1 : pos);
+            prefetch_l2(a.cosSin + pos * a.r + (STYLE == kNeox ? 8 : 4) * i);
+        }
+    }
+    grid_dependency_sync<POL>();
+    const L2Policies pol = make_policies<POL>();
 
     uint4 xa[IPT] = {}, xb[IPT] = {};
 #pragma unroll

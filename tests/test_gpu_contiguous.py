@@ -175,3 +175,45 @@ def test_config_written_slots_and_untouched(name):
         compare(g_rows, o_rows, cache_rotated((1,) + o_rows.shape, case.r)[0], f"{name} cache b={b}")
         written += len(slots) * 2 * case.Hkv * case.D
     assert _count_not_sentinel(cache) == written
+
+
+@pytest.mark.parametrize("B,S", [(2, 7), (3, 600)])
+def test_dependent_back_to_back_calls(B, S):
+    """Each call consumes the previous call's in-place output. Small launches
+    are dependent launches that prefetch before waiting on the previous grid,
+    large ones are plain launches; either way every call must see the previous
+    result. Three calls issued back to back, and replayed from a CUDA graph,
+    must give the bytes of three calls separated by host synchronisation."""
+    import rope_kv_cache_gb300 as rk
+    case = workloads.make_packed(B, S, 8, 2, 128, 128, 1024, NEOX, 1e4, seed=33,
+                                 cache_init="sentinel")
+    cs = to_dev(case.cos_sin)
+
+    def run(mode):
+        qkv = to_dev(case.qkv)
+        cache = to_dev(case.new_cache())
+        if mode == "graph":
+            s = torch.cuda.Stream()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                for _ in range(3):
+                    rk.rope_write_kv_packed(cs, qkv, cache, case.Hq, case.Hkv, case.style,
+                                            stream=torch.cuda.current_stream())
+            qkv.copy_(to_dev(case.qkv))
+            cache.copy_(to_dev(case.new_cache()))
+            torch.cuda.synchronize()
+            g.replay()
+        else:
+            for _ in range(3):
+                rk.rope_write_kv_packed(cs, qkv, cache, case.Hq, case.Hkv, case.style)
+                if mode == "synced":
+                    torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        return to_host_bits(qkv), to_host_bits(cache)
+
+    ref_qkv, ref_cache = run("synced")
+    assert not np.array_equal(ref_qkv, case.qkv)
+    for mode in ("back_to_back", "graph"):
+        q, c = run(mode)
+        assert np.array_equal(q, ref_qkv), mode
+        assert np.array_equal(c, ref_cache), mode
