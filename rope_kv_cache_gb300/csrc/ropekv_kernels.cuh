@@ -491,14 +491,16 @@ __global__ void __launch_bounds__(256) rope_kv_token_kernel(const TokenArgs a)
             const int item = item0 + k * blockDim.x;
             const int head = item / kItemsPerHead;
             const bool qk = item < a.itemsPerToken && head < a.Hq + a.Hkv;
-            float fa[8], fb[8];
-            unpack8(xa[k], fa);
-            unpack8(xb[k], fb);
+            uint32_t* wa_ = reinterpret_cast<uint32_t*>(&xa[k]);
+            uint32_t* wb_ = reinterpret_cast<uint32_t*>(&xb[k]);
             float ss = 0.0f;
             if (qk) {
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    ss = fmaf(fa[j], fa[j], fmaf(fb[j], fb[j], ss));
+                for (int q = 0; q < 4; ++q) {
+                    const float2 x = __half22float2(h2(wa_[q]));
+                    const float2 y = __half22float2(h2(wb_[q]));
+                    ss = fmaf(x.x, x.x, fmaf(x.y, x.y, fmaf(y.x, y.x, fmaf(y.y, y.y, ss))));
+                }
             }
             // all lanes take part: a head's lanes are aligned groups of D/16
 #pragma unroll
@@ -508,19 +510,42 @@ __global__ void __launch_bounds__(256) rope_kv_token_kernel(const TokenArgs a)
                 continue;
             const float inv = rsqrtf(ss * (1.0f / D) + a.eps);
             const bool isQ = head < a.Hq;
-            float w[8];
-            unpack8(isQ ? wqa : wka, w);
+            uint4 wA = isQ ? wqa : wka;
+            uint4 wB = isQ ? wqb : wkb;
+            uint32_t* wA_ = reinterpret_cast<uint32_t*>(&wA);
+            uint32_t* wB_ = reinterpret_cast<uint32_t*>(&wB);
+            // one half2 word of each vector at a time: normalize, rotate, pack
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                fa[j] = fa[j] * inv * w[j];
-            unpack8(isQ ? wqb : wkb, w);
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                fb[j] = fb[j] * inv * w[j];
-            if (rotItem)
-                rotate_item_f32<STYLE>(fa, fb, c, sn);
-            xa[k] = pack8(fa);
-            xb[k] = pack8(fb);
+            for (int q = 0; q < 4; ++q) {
+                float2 x = __half22float2(h2(wa_[q]));
+                float2 y = __half22float2(h2(wb_[q]));
+                const float2 u = __half22float2(h2(wA_[q]));
+                const float2 v = __half22float2(h2(wB_[q]));
+                x.x = x.x * inv * u.x;
+                x.y = x.y * inv * u.y;
+                y.x = y.x * inv * v.x;
+                y.y = y.y * inv * v.y;
+                if (rotItem) {
+                    if (STYLE == kNeox) {
+                        // dims 2q, 2q+1 of vector a pair with the same dims of b
+                        const float c0 = c[2 * q], c1 = c[2 * q + 1];
+                        const float s0 = sn[2 * q], s1 = sn[2 * q + 1];
+                        const float ax = fmaf(x.x, c0, -(y.x * s0));
+                        const float ay = fmaf(x.y, c1, -(y.y * s1));
+                        const float bx = fmaf(y.x, c0, x.x * s0);
+                        const float by = fmaf(y.y, c1, x.y * s1);
+                        x = make_float2(ax, ay);
+                        y = make_float2(bx, by);
+                    } else {
+                        // word q is one (2j, 2j+1) pair: frequency q in a, 4 + q in b
+                        x = make_float2(fmaf(x.x, c[q], -(x.y * sn[q])), fmaf(x.y, c[q], x.x * sn[q]));
+                        y = make_float2(fmaf(y.x, c[4 + q], -(y.y * sn[4 + q])),
+                                        fmaf(y.y, c[4 + q], y.x * sn[4 + q]));
+                    }
+                }
+                h2(wa_[q]) = __floats2half2_rn(x.x, x.y);
+                h2(wb_[q]) = __floats2half2_rn(y.x, y.y);
+            }
         }
     }
 
