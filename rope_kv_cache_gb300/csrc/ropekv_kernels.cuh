@@ -419,6 +419,7 @@ __global__ void __launch_bounds__(256) rope_kv_token_kernel(const TokenArgs a)
     item_vectors<D>(i, a.r, va, vb);
     const uint16_t* tokIn = a.qkv + (size_t)tok * H * D;
 
+    int specPos = -1;  // speculative position (prefetch prologue only)
     if ((POL & kPdl) && (POL & kPrefetch)) {
 #pragma unroll
         for (int k = 0; k < IPT; ++k) {
@@ -435,10 +436,22 @@ __global__ void __launch_bounds__(256) rope_kv_token_kernel(const TokenArgs a)
             pos = min(max(pos, 0), a.csSeq - 1);
             const int bc = (a.csBatch == 1) ? 0 : b;
             prefetch_l2(a.cosSin + ((size_t)bc * a.csSeq + pos) * a.r + (STYLE == kNeox ? 8 : 4) * i);
+            specPos = pos;
         }
     }
     grid_dependency_sync<POL>();
     const L2Policies pol = make_policies<POL>();
+    const bool rotItem = i < (a.r >> 4);
+    const int bcRow = (a.csBatch == 1) ? 0 : b;
+    float c[8], sn[8];
+    // After the wait every load sees the previous grid's writes. The cos/sin
+    // row of the speculative position is loaded now, in parallel with the
+    // position itself; it is kept only if the position turns out the same.
+    // (Measured: 256 decode tokens 2.46 -> 2.38 us; the FP8 and normalized
+    // variants were slower with it, so they load after the position.)
+    if (!NORM && !FP8 && specPos >= 0 && rotItem)
+        load_cos_sin<STYLE, POL>(a.cosSin + ((size_t)bcRow * a.csSeq + specPos) * a.r, i, a.r, c,
+                                 sn, pol);
 
     // 1. this thread's QKV vectors (independent of the position chain)
     uint4 xa[IPT] = {}, xb[IPT] = {};
@@ -470,12 +483,10 @@ __global__ void __launch_bounds__(256) rope_kv_token_kernel(const TokenArgs a)
             return;  // skipped token: nothing written
     }
 
-    // 3. cos/sin for this thread's frequencies
-    float c[8], sn[8];
-    const bool rotItem = i < (a.r >> 4);
-    if (rotItem) {
-        const int bc = (a.csBatch == 1) ? 0 : b;
-        const float* row = a.cosSin + ((size_t)bc * a.csSeq + pos) * a.r;
+    // 3. cos/sin for this thread's frequencies (unless the speculative
+    // position's row, already loaded, is the right one)
+    if (rotItem && (NORM || FP8 || pos != specPos)) {
+        const float* row = a.cosSin + ((size_t)bcRow * a.csSeq + pos) * a.r;
         load_cos_sin<STYLE, POL>(row, i, a.r, c, sn, pol);
     }
 
@@ -763,6 +774,8 @@ __global__ void __launch_bounds__(256) rope_kv_slotmap_kernel(const SlotMapArgs 
     }
     grid_dependency_sync<POL>();
     const L2Policies pol = make_policies<POL>();
+    const bool rotItem = i < (a.r >> 4);
+    float c[8], sn[8];
 
     uint4 xa[IPT] = {}, xb[IPT] = {};
 #pragma unroll
@@ -788,8 +801,6 @@ __global__ void __launch_bounds__(256) rope_kv_slotmap_kernel(const SlotMapArgs 
     const int64_t slot = __ldg(a.slots + tok);
     const bool kvOk = slot >= 0 && slot < a.numSlots;
 
-    float c[8], sn[8];
-    const bool rotItem = i < (a.r >> 4);
     if (rotItem)
         load_cos_sin<STYLE, POL>(a.cosSin + pos * a.r, i, a.r, c, sn, pol);
 
