@@ -24,8 +24,11 @@
  *     are float; indices are int32_t. All tensors are dense, row-major, in the
  *     layouts stated per call.
  *   - Every tensor pointer is a DEVICE pointer owned by the caller and must be
- *     16-byte aligned. The library allocates nothing, keeps no state between
- *     calls and never synchronises; results are ready when the stream says so.
+ *     16-byte aligned. The library allocates nothing and never synchronises;
+ *     results are ready when the stream says so. Its only state is a record,
+ *     per kernel and device, that the kernel's dynamic shared memory limit was
+ *     raised: decode-sized launches (fewer than 1024 tokens) reserve shared
+ *     memory they do not use so that their CTAs spread over all SMs.
  *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *     stream). Calls are asynchronous and may be captured in a CUDA graph.
  *   - cos/sin rows hold rotaryDim floats: cos_0..cos_{r/2-1} then

@@ -1,9 +1,12 @@
 // ropekv_api.cu -- the C ABI of libropekv.so: host-side argument checks, the
 // choice of kernel instantiation and launch shape, and one launch per call on
 // the caller's stream. Declarations and the meaning of every argument are in
-// include/ropekv.h. Nothing here allocates, synchronises or keeps state.
+// include/ropekv.h. Nothing here allocates or synchronises; the only state is
+// a per-kernel record of the devices on which its dynamic shared memory limit
+// was raised (see residency_smem).
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <stdint.h>
 
 #include "ropekv.h"
@@ -39,31 +42,33 @@ int check_head_dims(int32_t D, int32_t r)
 //     (128 items = 16 heads of 128 dims per CTA) keep the CTA launch rate and
 //     the bytes in flight per SM balanced; bigger CTAs lose 2-5 % on the
 //     shorter tree/paged launches, smaller ones run into the CTA launch rate;
-//   * small launches (decode): one item per thread, up to 192 items per CTA,
-//     which spreads the few tokens over more SMs.
+//   * small launches (decode): two items per thread and up to 384 items per
+//     CTA (one CTA per decode token of 32 + 2 x 8 heads of 128 dims), spread
+//     over the SMs by the residency cap below (256 decode tokens, plain /
+//     QK-normalized: 2.40 / 2.78 us with one item per thread and no cap,
+//     2.07 / 2.57 us this way).
 // Blocks are whole warps; a warp's size is a multiple of every D/16, which
 // keeps each thread on one item index.
 struct Shape {
     int threads;
     int ipt;
     int ctasPerUnit;
+    bool small;  // dependent launch with the prefetch prologue and a residency cap
 };
 
 Shape pick_shape(int items, long long units, bool heavy = false)
 {
     Shape sh;
     int perCta;
-    if (heavy) {
+    sh.small = units < 1024;
+    if (sh.small) {
+        sh.ipt = 2;
+        perCta = 384;
+    } else {
         // the QK-normalized call does ~3x the arithmetic per byte: more items
         // per thread keep more loads in flight while it computes (measured)
-        sh.ipt = units >= 1024 ? 4 : 1;
-        perCta = units >= 1024 ? 128 : 64;
-    } else if (units >= 1024) {
-        sh.ipt = 2;
+        sh.ipt = heavy ? 4 : 2;
         perCta = 128;
-    } else {
-        sh.ipt = 1;
-        perCta = 192;
     }
     sh.ctasPerUnit = (items + perCta - 1) / perCta;
     const int per = (items + sh.ctasPerUnit * sh.ipt - 1) / (sh.ctasPerUnit * sh.ipt);
@@ -73,12 +78,11 @@ Shape pick_shape(int items, long long units, bool heavy = false)
 
 // Kernel policies (see ropekv_kernels.cuh), measured on GB300:
 //   * every launch: streaming L2 hints on activations and cache rows;
-//   * one-item-per-thread (decode-sized) token and slot-mapping launches:
-//     programmatic dependent launch with the L2 prefetch prologue, which takes
-//     the position -> cos/sin chain and the input reads off the critical path
+//   * small (decode-sized) token and slot-mapping launches: programmatic
+//     dependent launch with the L2 prefetch prologue, which takes the
+//     position -> cos/sin chain and the input reads off the critical path
 //     while the previous kernel in the stream drains (256 decode tokens:
-//     3.01 -> 2.47 us per launch). Dependent launch alone, without the
-//     prologue, was slightly slower on these small grids;
+//     3.01 -> 2.47 us per launch), plus the residency cap below;
 //   * larger token launches of at most kPdlMaxCtas CTAs: dependent launch only
 //     (tree, 12288 CTAs: 16.56 -> 16.17 us). Above that, and for the paged
 //     kernels, no dependent launch: it caps the CTA launch rate near one CTA per
@@ -93,12 +97,12 @@ constexpr long long kPdlMaxCtas = 12288;
 
 template <typename Args>
 void launch_k(void (*kern)(Args), unsigned grid, int threads, cudaStream_t st, bool pdl,
-              const Args& a)
+              const Args& a, size_t smem = 0)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3((unsigned)threads);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -108,20 +112,82 @@ void launch_k(void (*kern)(Args), unsigned grid, int threads, cudaStream_t st, b
     (void)cudaLaunchKernelEx(&cfg, kern, a);
 }
 
-template <int D, int STYLE, int MODE, int IPT, bool NORM, bool FP8>
-void launch_token_variant(const TokenArgs& a, unsigned grid, int threads, cudaStream_t st)
+// Residency cap of a small dependent launch. A launch that starts while its
+// predecessor still runs gets its CTAs placed densely: a per-warp timer trace
+// of 512 decode CTAs of 192 threads found them on 61-66 of the 152 SMs, up to
+// ten per SM, and the launch then lasts as long as the most loaded SMs take to
+// issue their work. Dynamic shared memory that the kernel does not use, sized
+// so that at most ceil(grid / SMs) CTAs fit on one SM, spreads the CTAs over
+// the GPU (256 decode tokens: 2.40 -> 2.07 us per launch). Returns 0 (no cap)
+// for grids of more than 8 CTAs per SM or when the device cannot be queried;
+// *optin receives the device's per-block shared memory limit.
+size_t residency_smem(unsigned grid, int* optin)
 {
-    if constexpr (IPT == 1) {
-        launch_k(ropekv::rope_kv_token_kernel<D, STYLE, MODE, 1, kPolSmall, NORM, FP8>, grid,
-                 threads, st, true, a);
-    } else {
-        if (grid <= kPdlMaxCtas)
-            launch_k(ropekv::rope_kv_token_kernel<D, STYLE, MODE, IPT, kPolPdl, NORM, FP8>, grid,
-                     threads, st, true, a);
-        else
-            launch_k(ropekv::rope_kv_token_kernel<D, STYLE, MODE, IPT, kPolLarge, NORM, FP8>,
-                     grid, threads, st, false, a);
+    int dev = 0, sms = 0, perSm = 0, reserved = 0;
+    *optin = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&perSm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) !=
+            cudaSuccess || sms <= 0) {
+        (void)cudaGetLastError();
+        return 0;
     }
+    const unsigned cap = (grid + (unsigned)sms - 1) / (unsigned)sms;
+    if (cap == 0 || cap > 8)
+        return 0;
+    long long bytes = (long long)perSm / cap - reserved;
+    if (bytes > *optin)
+        bytes = *optin;
+    return bytes > 0 ? (size_t)(bytes & ~255LL) : 0;
+}
+
+// Launch of a small dependent kernel with its residency cap. A kernel's
+// dynamic shared memory limit is raised from the default 48 KB to the
+// device's maximum once per device (one bit per device ordinal below 64;
+// higher ordinals raise it on every call) -- the only state the library keeps.
+template <auto Kern, typename Args>
+void launch_small(unsigned grid, int threads, cudaStream_t st, const Args& a)
+{
+    int optin = 0;
+    size_t smem = residency_smem(grid, &optin);
+    if (smem > 48 * 1024) {
+        static std::atomic<unsigned long long> raised{0};
+        int dev = 0;
+        (void)cudaGetDevice(&dev);
+        const unsigned long long bit = (dev >= 0 && dev < 64) ? 1ULL << dev : 0;
+        if (!bit || !(raised.load(std::memory_order_relaxed) & bit)) {
+            if (cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) ==
+                cudaSuccess) {
+                raised.fetch_or(bit, std::memory_order_relaxed);
+            } else {
+                (void)cudaGetLastError();
+                smem = 0;  // launch without the cap rather than fail
+            }
+        }
+    }
+    launch_k(Kern, grid, threads, st, true, a, smem);
+}
+
+template <int D, int STYLE, int MODE, int IPT, bool NORM, bool FP8>
+void launch_token_variant(const TokenArgs& a, unsigned grid, const Shape& sh, cudaStream_t st)
+{
+    if constexpr (IPT == 2) {
+        if (sh.small) {
+            launch_small<ropekv::rope_kv_token_kernel<D, STYLE, MODE, IPT, kPolSmall, NORM, FP8>>(
+                grid, sh.threads, st, a);
+            return;
+        }
+    }
+    if (grid <= kPdlMaxCtas)
+        launch_k(ropekv::rope_kv_token_kernel<D, STYLE, MODE, IPT, kPolPdl, NORM, FP8>, grid,
+                 sh.threads, st, true, a);
+    else
+        launch_k(ropekv::rope_kv_token_kernel<D, STYLE, MODE, IPT, kPolLarge, NORM, FP8>, grid,
+                 sh.threads, st, false, a);
 }
 
 template <int D, int STYLE, int MODE, int IPT>
@@ -130,29 +196,27 @@ void launch_token(const TokenArgs& a, long long tokens, const Shape& sh, cudaStr
     const unsigned grid = (unsigned)(tokens * sh.ctasPerUnit);
     if constexpr (MODE == ropekv::kContinuous) {
         if (a.qNormW != nullptr) {
-            launch_token_variant<D, STYLE, MODE, IPT, true, false>(a, grid, sh.threads, st);
+            launch_token_variant<D, STYLE, MODE, IPT, true, false>(a, grid, sh, st);
             return;
         }
         if (a.cache8 != nullptr) {
             if constexpr (IPT != 4)
-                launch_token_variant<D, STYLE, MODE, IPT, false, true>(a, grid, sh.threads, st);
+                launch_token_variant<D, STYLE, MODE, IPT, false, true>(a, grid, sh, st);
             return;
         }
     }
     if constexpr (IPT != 4)
-        launch_token_variant<D, STYLE, MODE, IPT, false, false>(a, grid, sh.threads, st);
+        launch_token_variant<D, STYLE, MODE, IPT, false, false>(a, grid, sh, st);
 }
 
 template <int D, int STYLE, int MODE>
 void dispatch_ipt(const TokenArgs& a, long long tokens, const Shape& sh, cudaStream_t st)
 {
-    if (sh.ipt == 2) {
-        launch_token<D, STYLE, MODE, 2>(a, tokens, sh, st);
-    } else if (sh.ipt == 4) {
+    if (sh.ipt == 4) {
         if constexpr (MODE == ropekv::kContinuous)
             launch_token<D, STYLE, MODE, 4>(a, tokens, sh, st);  // the normalized call only
     } else {
-        launch_token<D, STYLE, MODE, 1>(a, tokens, sh, st);
+        launch_token<D, STYLE, MODE, 2>(a, tokens, sh, st);
     }
 }
 
@@ -180,13 +244,10 @@ void dispatch_token(const TokenArgs& a, int D, int style, long long tokens, cons
 template <int D, int STYLE, bool FUSED>
 void launch_paged(const PagedArgs& a, long long rows, const Shape& sh, cudaStream_t st)
 {
+    // pick_shape gives the paged rows (never "heavy") two items per thread
     const unsigned grid = (unsigned)(rows * sh.ctasPerUnit);
-    if (sh.ipt == 2)
-        launch_k(ropekv::paged_delta_kernel<D, STYLE, 2, kPolLarge, FUSED>, grid, sh.threads, st,
-                 false, a);
-    else
-        launch_k(ropekv::paged_delta_kernel<D, STYLE, 1, kPolLarge, FUSED>, grid, sh.threads, st,
-                 false, a);
+    launch_k(ropekv::paged_delta_kernel<D, STYLE, 2, kPolLarge, FUSED>, grid, sh.threads, st,
+             false, a);
 }
 
 template <bool FUSED>
@@ -638,16 +699,16 @@ int rope_write_kv_slot_mapping(const float* cosSin, const int64_t* positions, co
     const bool gptj = style == ROPEKV_GPTJ;
 #define ROPEKV_SLOTMAP_LAUNCH(DD)                                                            \
     do {                                                                                   \
-        if (sh.ipt == 2)                                                                   \
+        if (!sh.small)                                                                     \
             gptj ? launch_k(ropekv::rope_kv_slotmap_kernel<DD, ropekv::kGptj, 2, kPolLarge>, \
                             grid, sh.threads, st, false, a)                                \
                  : launch_k(ropekv::rope_kv_slotmap_kernel<DD, ropekv::kNeox, 2, kPolLarge>, \
                             grid, sh.threads, st, false, a);                               \
         else                                                                               \
-            gptj ? launch_k(ropekv::rope_kv_slotmap_kernel<DD, ropekv::kGptj, 1, kPolSmall>, \
-                            grid, sh.threads, st, true, a)                                 \
-                 : launch_k(ropekv::rope_kv_slotmap_kernel<DD, ropekv::kNeox, 1, kPolSmall>, \
-                            grid, sh.threads, st, true, a);                                \
+            gptj ? launch_small<ropekv::rope_kv_slotmap_kernel<DD, ropekv::kGptj, 2, kPolSmall>>( \
+                       grid, sh.threads, st, a)                                            \
+                 : launch_small<ropekv::rope_kv_slotmap_kernel<DD, ropekv::kNeox, 2, kPolSmall>>( \
+                       grid, sh.threads, st, a);                                           \
     } while (0)
     switch (headDim) {
     case 64: ROPEKV_SLOTMAP_LAUNCH(64); break;

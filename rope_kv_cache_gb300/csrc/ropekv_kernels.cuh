@@ -269,6 +269,24 @@ __device__ __forceinline__ void load_cos_sin(const float* row, int i, int r, flo
     s[4] = f.x; s[5] = f.y; s[6] = f.z; s[7] = f.w;
 }
 
+// L2 prefetch of exactly the cos/sin values load_cos_sin reads for item i
+// (a prefetch covers the 32-byte sector of its address; the row starts on a
+// 64-byte boundary, so NeoX's 8 cos and 8 sin floats are one sector each).
+template <int STYLE>
+__device__ __forceinline__ void prefetch_cos_sin(const float* row, int i, int r)
+{
+    const int h = r >> 1;
+    if (STYLE == kNeox) {
+        prefetch_l2(row + 8 * i);
+        prefetch_l2(row + h + 8 * i);
+    } else {
+        prefetch_l2(row + 4 * i);
+        prefetch_l2(row + 4 * i + (r >> 2));
+        prefetch_l2(row + h + 4 * i);
+        prefetch_l2(row + h + 4 * i + (r >> 2));
+    }
+}
+
 // NeoX: va holds dims 8i..8i+7 (first half), vb the partner dims 8i+r/2...;
 // a' = a*c - b*s, b' = b*c + a*s with the frequency of the pair.
 __device__ __forceinline__ void rotate_neox(uint4& va, uint4& vb, const float c[8],
@@ -435,7 +453,7 @@ __global__ void __launch_bounds__(256) rope_kv_token_kernel(const TokenArgs a)
                                       : load_int_l2(a.endLens + b) - a.S + s;
             pos = min(max(pos, 0), a.csSeq - 1);
             const int bc = (a.csBatch == 1) ? 0 : b;
-            prefetch_l2(a.cosSin + ((size_t)bc * a.csSeq + pos) * a.r + (STYLE == kNeox ? 8 : 4) * i);
+            prefetch_cos_sin<STYLE>(a.cosSin + ((size_t)bc * a.csSeq + pos) * a.r, i, a.r);
             specPos = pos;
         }
     }
@@ -769,7 +787,7 @@ __global__ void __launch_bounds__(256) rope_kv_slotmap_kernel(const SlotMapArgs 
             int64_t pos;
             asm volatile("ld.global.cg.s64 %0, [%1];" : "=l"(pos) : "l"(a.positions + tok));
             pos = pos < 0 ? 0 : (pos >= a.csRows ? a.csRows - 1 : pos);
-            prefetch_l2(a.cosSin + pos * a.r + (STYLE == kNeox ? 8 : 4) * i);
+            prefetch_cos_sin<STYLE>(a.cosSin + pos * a.r, i, a.r);
         }
     }
     grid_dependency_sync<POL>();

@@ -217,3 +217,18 @@ def test_dependent_back_to_back_calls(B, S):
         q, c = run(mode)
         assert np.array_equal(q, ref_qkv), mode
         assert np.array_equal(c, ref_cache), mode
+
+
+@pytest.mark.parametrize("tokens", [1, 152, 153, 450, 608, 609, 1000, 1023])
+@pytest.mark.parametrize("norm", [False, True])
+def test_small_launch_residency_caps(tokens, norm):
+    """Decode-sized launches (fewer than 1024 tokens) reserve dynamic shared
+    memory so that at most ceil(CTAs / SMs) CTAs share an SM: 1, 2, 3, 4, 5
+    and 7 CTAs per SM here (the normalized call, two CTAs per token, also
+    crosses the 8-per-SM limit above which no memory is reserved). Every cap
+    gives the oracle's result."""
+    case = workloads.make_continuous(tokens, 1, 8, 2, 128, 128, 16, NEOX, 5e5, seed=4000 + tokens,
+                                     name=f"caps{tokens}")
+    if norm:
+        case.norm = workloads.norm_weights(4000 + tokens, 128)
+    check_contiguous(case)

@@ -86,6 +86,18 @@ def test_small_cases(idx):
         assert np.any(o_cache[:, 0] == 0x7E) or np.any(o_cache[:, 0] == 0xFE) or True
 
 
+@pytest.mark.parametrize("tokens", [1, 153, 700])
+def test_small_launch_residency_caps(tokens):
+    """Decode-sized FP8 launches with 1, 2 and 5 CTAs per SM (one per token)."""
+    case = workloads.make_continuous(tokens, 1, 8, 2, 128, 128, 16, NEOX, 5e5, seed=800 + tokens,
+                                     name=f"fp8_caps{tokens}")
+    case.fp8_scales = (0.05, 0.04)
+    g_cache, g_q = _run(case)
+    o_cache, o_q = _oracle(case)
+    compare(g_q, o_q, qout_rotated(o_q.shape, 128), f"{case.name} qOut")
+    compare_e4m3(g_cache, o_cache, f"{case.name} cache")
+
+
 def test_skips_and_saturation():
     case = workloads.make_continuous(4, 6, 4, 2, 128, 128, 32, NEOX, 5e5, seed=21,
                                      end_lens=[3, 35, 32, 20], cs_seq=30, name="fp8_skips")

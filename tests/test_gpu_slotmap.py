@@ -64,6 +64,8 @@ SMALL = [
     ([7, 7, 7], 16, 1, 256, 128, NEOX, 4, 20, True, True),
     ([600, 500], 4, 2, 128, 64, GPTJ, 64, 24, True, False),   # >= 1024 tokens
     ([3], 64, 64, 128, 128, NEOX, 2, 4, True, False),         # 192 heads
+    ([1] * 153, 8, 2, 128, 128, NEOX, 4, 160, False, False),  # 153 one-token CTAs: 2 per SM
+    ([1] * 700, 8, 2, 128, 128, GPTJ, 4, 704, True, False),   # 700: 5 per SM
 ]
 
 
