@@ -38,15 +38,19 @@ int check_head_dims(int32_t D, int32_t r)
 
 // Launch shape for `units` tokens (or rows) of `items` items each.
 // Measured on GB300 over the prefill, decode, tree and paged workloads:
-//   * large launches (>= 1024 units): 64-thread CTAs with two items per thread
-//     (128 items = 16 heads of 128 dims per CTA) keep the CTA launch rate and
-//     the bytes in flight per SM balanced; bigger CTAs lose 2-5 % on the
-//     shorter tree/paged launches, smaller ones run into the CTA launch rate;
-//   * small launches (decode): two items per thread and up to 384 items per
-//     CTA (one CTA per decode token of 32 + 2 x 8 heads of 128 dims), spread
-//     over the SMs by the residency cap below (256 decode tokens, plain /
-//     QK-normalized: 2.40 / 2.78 us with one item per thread and no cap,
-//     2.07 / 2.57 us this way).
+//   * two items per thread and up to 384 items per CTA: one 192-thread CTA per
+//     token of 32 + 2 x 8 heads of 128 dims, one 64-thread CTA per paged row
+//     of 8 + 8 heads. With dependent launch, the 8192-token prefill takes
+//     30.30 us this way against 30.60 us with three 64-thread CTAs per token
+//     (no dependent launch: at that CTA count its launch-rate cap hurt), and
+//     the 4096-token tree 15.96 against 16.02 us;
+//   * small launches (< 1024 units, decode) add the residency cap below
+//     (256 decode tokens, plain / QK-normalized: 2.40 / 2.78 us with one item
+//     per thread in 192- / 64-thread CTAs and no cap, 2.07 / 2.57 us this way);
+//   * the large QK-normalized launch, ~3x the arithmetic per byte, keeps 32
+//     threads x 4 items per CTA (more loads in flight per thread; 96 x 4 with
+//     dependent launch: 31.60 us, the same), and the large FP8-cache launch
+//     64 x 2 (8192 tokens: 28.53 us; 192 x 2 with dependent launch: 29.14 us).
 // Blocks are whole warps; a warp's size is a multiple of every D/16, which
 // keeps each thread on one item index.
 struct Shape {
@@ -56,18 +60,21 @@ struct Shape {
     bool small;  // dependent launch with the prefetch prologue and a residency cap
 };
 
-Shape pick_shape(int items, long long units, bool heavy = false)
+enum class Work { kPlain, kNorm, kFp8 };
+
+Shape pick_shape(int items, long long units, Work work = Work::kPlain)
 {
     Shape sh;
     int perCta;
     sh.small = units < 1024;
-    if (sh.small) {
+    if (sh.small || work == Work::kPlain) {
         sh.ipt = 2;
         perCta = 384;
+    } else if (work == Work::kNorm) {
+        sh.ipt = 4;
+        perCta = 128;
     } else {
-        // the QK-normalized call does ~3x the arithmetic per byte: more items
-        // per thread keep more loads in flight while it computes (measured)
-        sh.ipt = heavy ? 4 : 2;
+        sh.ipt = 2;
         perCta = 128;
     }
     sh.ctasPerUnit = (items + perCta - 1) / perCta;
@@ -83,17 +90,25 @@ Shape pick_shape(int items, long long units, bool heavy = false)
 //     position -> cos/sin chain and the input reads off the critical path
 //     while the previous kernel in the stream drains (256 decode tokens:
 //     3.01 -> 2.47 us per launch), plus the residency cap below;
-//   * larger token launches of at most kPdlMaxCtas CTAs: dependent launch only
-//     (tree, 12288 CTAs: 16.56 -> 16.17 us). Above that, and for the paged
-//     kernels, no dependent launch: it caps the CTA launch rate near one CTA per
-//     nanosecond, which starves grids of many short CTAs (the fused paged
-//     update, half of whose rows are padding, went from 13.9 to 17.3 us).
+//   * larger token and slot-mapping launches: dependent launch without the
+//     prologue (tree: 16.56 -> 16.17 us) when the grid has at most
+//     kPdlMaxCtas CTAs or its CTAs cover at least 256 items. The attribute
+//     caps the CTA launch rate near one CTA per nanosecond, which starves
+//     grids of many short CTAs (a 49 152-CTA prefill of 128-item CTAs: 29.9 ->
+//     49.8 us); a 256-item CTA moves ~16 KB, more than HBM delivers in a
+//     nanosecond. The paged kernels (128-item CTAs, many of them padding or
+//     short) launch without it (the fused update: 13.9 -> 17.3 us with it).
 // Kernels that do not wait on the previous grid (the DFlash metadata and
 // gather kernels) never get the dependent-launch attribute.
 constexpr int kPolLarge = ropekv::kStreamHint;
 constexpr int kPolPdl = ropekv::kStreamHint | ropekv::kPdl;
 constexpr int kPolSmall = ropekv::kStreamHint | ropekv::kPdl | ropekv::kPrefetch;
 constexpr long long kPdlMaxCtas = 12288;
+
+bool pdl_allowed(unsigned grid, const Shape& sh)
+{
+    return grid <= kPdlMaxCtas || sh.threads * sh.ipt >= 256;
+}
 
 template <typename Args>
 void launch_k(void (*kern)(Args), unsigned grid, int threads, cudaStream_t st, bool pdl,
@@ -182,7 +197,7 @@ void launch_token_variant(const TokenArgs& a, unsigned grid, const Shape& sh, cu
             return;
         }
     }
-    if (grid <= kPdlMaxCtas)
+    if (pdl_allowed(grid, sh))
         launch_k(ropekv::rope_kv_token_kernel<D, STYLE, MODE, IPT, kPolPdl, NORM, FP8>, grid,
                  sh.threads, st, true, a);
     else
@@ -344,7 +359,10 @@ TokenArgs token_args(const ropekv_dims* d)
 int launch_contiguous(TokenArgs a, const ropekv_dims* d, long long tokens, int mode,
                       cudaStream_t st)
 {
-    const Shape sh = pick_shape(a.itemsPerToken, tokens, a.qNormW != nullptr);
+    const Shape sh = pick_shape(a.itemsPerToken, tokens,
+                                a.qNormW != nullptr  ? Work::kNorm
+                                : a.cache8 != nullptr ? Work::kFp8
+                                                      : Work::kPlain);
     if (tokens * sh.ctasPerUnit > 0x7FFFFFFFLL)
         return ROPEKV_ERR_SHAPE;
     a.ctasPerToken = sh.ctasPerUnit;
@@ -699,11 +717,16 @@ int rope_write_kv_slot_mapping(const float* cosSin, const int64_t* positions, co
     const bool gptj = style == ROPEKV_GPTJ;
 #define ROPEKV_SLOTMAP_LAUNCH(DD)                                                            \
     do {                                                                                   \
-        if (!sh.small)                                                                     \
+        if (!sh.small && !pdl_allowed(grid, sh))                                           \
             gptj ? launch_k(ropekv::rope_kv_slotmap_kernel<DD, ropekv::kGptj, 2, kPolLarge>, \
                             grid, sh.threads, st, false, a)                                \
                  : launch_k(ropekv::rope_kv_slotmap_kernel<DD, ropekv::kNeox, 2, kPolLarge>, \
                             grid, sh.threads, st, false, a);                               \
+        else if (!sh.small)                                                                \
+            gptj ? launch_k(ropekv::rope_kv_slotmap_kernel<DD, ropekv::kGptj, 2, kPolPdl>, \
+                            grid, sh.threads, st, true, a)                                 \
+                 : launch_k(ropekv::rope_kv_slotmap_kernel<DD, ropekv::kNeox, 2, kPolPdl>, \
+                            grid, sh.threads, st, true, a);                                \
         else                                                                               \
             gptj ? launch_small<ropekv::rope_kv_slotmap_kernel<DD, ropekv::kGptj, 2, kPolSmall>>( \
                        grid, sh.threads, st, a)                                            \

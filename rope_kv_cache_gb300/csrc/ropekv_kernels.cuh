@@ -704,9 +704,11 @@ __global__ void __launch_bounds__(256) paged_delta_kernel(const PagedArgs a)
     const bool kOk = idK >= 0 && idK < a.numPages;
     const bool vOk = idV >= a.numPages && (int64_t)idV < 2 * (int64_t)a.numPages;
 
+    // cos/sin are loaded whether or not the K page is mapped, so that their
+    // address does not wait for the page-table lookup (measured ~1 % faster)
     float c[8], sn[8];
     const bool rotItem = i < (a.r >> 4);
-    if (rotItem && kOk) {
+    if (rotItem) {
         if (FUSED) {
             int state = -1;
             if (pos < a.cacheCapacity)
