@@ -232,3 +232,124 @@ def test_small_launch_residency_caps(tokens, norm):
     if norm:
         case.norm = workloads.norm_weights(4000 + tokens, 128)
     check_contiguous(case)
+
+
+@pytest.mark.parametrize("B,S", [(4, 1), (2, 600)])
+def test_mixed_dependent_chain(B, S):
+    """Four different entry points, each reading or overwriting what the one
+    before it wrote, issued back to back and replayed from a CUDA graph, give
+    the bytes of the same calls separated by host synchronisation: the packed
+    call rotates qkv in place and fills cache slots 0..S-1; the continuous call
+    reads that qkv, writes qOut and rewrites slots 5..S+4; the normalized call
+    reads qkv again and rewrites those slots; the slot-mapping call takes the
+    first qOut as its Q and the K/V heads of qkv as token-strided views.
+    (4, 1) runs every call as a small dependent launch with the prefetch
+    prologue and residency cap, (2, 600) as large ones."""
+    import rope_kv_cache_gb300 as rk
+    Hq, Hkv, D = 8, 2, 128
+    H, T = Hq + 2 * Hkv, B * S
+    case = workloads.make_packed(B, S, Hq, Hkv, D, 128, 1024, NEOX, 1e4, seed=77,
+                                 cache_init="sentinel")
+    cs = to_dev(case.cos_sin)
+    end = torch.full((B,), S + 5, dtype=torch.int32, device="cuda:0")
+    qw, kw, eps = workloads.norm_weights(77, D)
+    qw, kw = to_dev(qw), to_dev(kw)
+    positions = (torch.arange(T, device="cuda:0", dtype=torch.int64) * 7) % 1000
+    slots = torch.arange(T, device="cuda:0", dtype=torch.int64).flip(0)
+    sent = np.uint16(workloads.SENTINEL).view(np.int16).item()
+
+    def run(mode):
+        qkv = to_dev(case.qkv)
+        cache = to_dev(case.new_cache())
+        qout = torch.zeros((B, S, Hq, D), dtype=torch.float16, device="cuda:0")
+        qout2 = torch.zeros_like(qout)
+        kc = torch.full((T, 1, Hkv, D), sent, dtype=torch.int16, device="cuda:0").view(torch.float16)
+        vc = kc.clone()
+        qo3 = torch.zeros((T, Hq, D), dtype=torch.float16, device="cuda:0")
+
+        def chain(stream):
+            rk.rope_write_kv_packed(cs, qkv, cache, Hq, Hkv, NEOX, stream=stream)
+            rk.rope_write_kv_continuous(cs, end, qkv, cache, qout, Hq, Hkv, NEOX, stream=stream)
+            rk.rope_write_kv_continuous_qknorm(cs, end, qkv, cache, qout2, qw, kw, eps, Hq, Hkv,
+                                               NEOX, stream=stream)
+            flat = qkv.view(T, H, D)
+            rk.rope_write_kv_slot_mapping(cs[0], positions, qout.view(T, Hq, D),
+                                          flat[:, Hq:Hq + Hkv], flat[:, Hq + Hkv:], slots, kc, vc,
+                                          qo3, style=NEOX, stream=stream)
+
+        if mode == "graph":
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=torch.cuda.Stream()):
+                chain(torch.cuda.current_stream())
+            qkv.copy_(to_dev(case.qkv))
+            cache.copy_(to_dev(case.new_cache()))
+            for t in (qout, qout2, qo3):
+                t.zero_()
+            kc.view(torch.int16).fill_(sent)
+            vc.view(torch.int16).fill_(sent)
+            torch.cuda.synchronize()
+            g.replay()
+        elif mode == "synced":
+            for step in range(4):
+                # the same calls one at a time, each completed before the next
+                calls = [
+                    lambda: rk.rope_write_kv_packed(cs, qkv, cache, Hq, Hkv, NEOX),
+                    lambda: rk.rope_write_kv_continuous(cs, end, qkv, cache, qout, Hq, Hkv, NEOX),
+                    lambda: rk.rope_write_kv_continuous_qknorm(cs, end, qkv, cache, qout2, qw, kw,
+                                                               eps, Hq, Hkv, NEOX),
+                    lambda: rk.rope_write_kv_slot_mapping(
+                        cs[0], positions, qout.view(T, Hq, D), qkv.view(T, H, D)[:, Hq:Hq + Hkv],
+                        qkv.view(T, H, D)[:, Hq + Hkv:], slots, kc, vc, qo3, style=NEOX),
+                ]
+                calls[step]()
+                torch.cuda.synchronize()
+        else:
+            chain(None)
+        torch.cuda.synchronize()
+        return [to_host_bits(t) for t in (qkv, cache, qout, qout2, kc, vc, qo3)]
+
+    ref = run("synced")
+    # every output was written (position 0 of the packed call is the identity,
+    # so qkv itself only changes when S > 1)
+    assert all(np.any(x != 0) for x in ref[2:4] + ref[6:])
+    assert not np.array_equal(ref[1], case.new_cache()) and np.all(ref[4] != workloads.SENTINEL)
+    for mode in ("back_to_back", "graph"):
+        got = run(mode)
+        for name, g_, r_ in zip(("qkv", "cache", "qout", "qout2", "kc", "vc", "qo3"), got, ref):
+            assert np.array_equal(g_, r_), f"{mode}: {name}"
+
+
+def test_first_call_inside_graph_capture():
+    """A decode-sized call made for the first time in a process while a CUDA
+    graph is being captured (the library then raises the kernel's shared
+    memory limit during the capture) is captured and replays correctly. Runs
+    in a fresh interpreter so that no earlier call has raised the limit."""
+    import os
+    import subprocess
+    import sys
+    code = r'''
+import sys
+sys.path.insert(0, "tests")
+import numpy as np, torch
+import workloads
+from parity import check_contiguous, run_oracle_contiguous, to_dev, to_host_bits
+import rope_kv_cache_gb300 as rk
+case = workloads.make_continuous(256, 1, 32, 8, 128, 128, 64, workloads.NEOX, 5e5, seed=91)
+cs, end, qkv = to_dev(case.cos_sin), to_dev(case.end_lens), to_dev(case.qkv)
+cache, qout = to_dev(case.new_cache()), to_dev(case.new_qout())
+g = torch.cuda.CUDAGraph()
+with torch.cuda.graph(g, stream=torch.cuda.Stream()):
+    rk.rope_write_kv_continuous(cs, end, qkv, cache, qout, case.Hq, case.Hkv, case.style,
+                                stream=torch.cuda.current_stream())
+g.replay()
+torch.cuda.synchronize()
+o_qkv, o_cache, o_qout = run_oracle_contiguous(case)
+from parity import compare, cache_rotated, qout_rotated
+compare(to_host_bits(qout), o_qout, qout_rotated(o_qout.shape, 128), "qOut")
+compare(to_host_bits(cache), o_cache, cache_rotated(o_cache.shape, 128), "cache")
+print("ok")
+'''
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout + r.stderr
