@@ -736,6 +736,7 @@ def main(argv=None):
         "data": "synthetic: seeded N(0,1) FP16 activations, FP32 RoPE table (no dataset, no weights)",
         "config": {"workload": DESCR.get(name, name), "tokens_per_step": tokens,
                    "bytes_per_step": bytes_step,
+                   "parallelism": f"one independent replica per GPU x{world} (no exchange)",
                    "l2": f"inputs larger than L2: ring of {ring} input sets, "
                          f"{ring * bytes_step / 1e6:.0f} MB > 2 x L2 ({l2 / 1e6:.0f} MB)"},
         "effective_gbs": achieved,
