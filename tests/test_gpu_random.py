@@ -7,7 +7,8 @@ outside the cache or table. Paged updates (20 seeds) and fused DFlash updates
 (20 seeds): random heads, dims, page size, pages per sequence, pool size,
 padding and unmapped pages, cos/sin source rows and state indices. Slot
 mapping (20 seeds): random sequence mixes, block sizes, strided or separate
-Q/K/V, optional kOut, skipped slots and positions past the table."""
+Q/K/V, optional kOut, skipped slots and positions past the table. FP8 cache
+(12 seeds): random shapes and K/V scales, some small enough to saturate."""
 import numpy as np
 import pytest
 
@@ -183,3 +184,44 @@ def test_random_slot_mapping(seed):
     compare(to_host_bits(qo), w[2], rot[None, None, :], f"{case.name} qOut")
     if with_kout:
         compare(to_host_bits(ko), w[3], rot[None, None, :], f"{case.name} kOut")
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_fp8(seed):
+    """Random continuous calls into an E4M3 cache: dims, pairing, heads,
+    ragged lengths, out-of-cache slots and K/V scales from 1/64 to 4 (small
+    scales saturate)."""
+    import oracle
+    import rope_kv_cache_gb300 as rk
+    from parity import compare, qout_rotated, to_dev, to_host_bits
+    from test_gpu_fp8 import compare_e4m3
+    rng = np.random.Generator(np.random.PCG64(50_000 + seed))
+    style = int(rng.integers(0, 2))
+    D = int(rng.choice([64, 128, 256]))
+    r = int(rng.choice([x for x in (16, 32, 64, 128, 256) if x <= D]))
+    Hkv = int(rng.choice([1, 2, 4, 8]))
+    Hq = Hkv * int(rng.choice([1, 2, 4]))
+    B = int(rng.integers(1, 5))
+    S = int(rng.choice([1, 3, 37, int(rng.integers(1, 600))]))
+    cap = S + int(rng.integers(0, 100))
+    end = rng.integers(S - 2, cap + 3, size=B).astype(np.int32)
+    case = workloads.make_continuous(B, S, Hq, Hkv, D, r, cap, style, 1e4, seed=50_000 + seed,
+                                     end_lens=end, name=f"rfp8_{seed}")
+    case.fp8_scales = (float(2.0 ** rng.integers(-6, 3)) * float(rng.choice([1.0, 0.7])),
+                       float(2.0 ** rng.integers(-6, 3)))
+    cache = torch.full(case.new_cache8().shape, workloads.SENTINEL8, dtype=torch.uint8,
+                       device="cuda:0")
+    qout = to_dev(case.new_qout())
+    ks, vs = case.fp8_scales
+    rk.rope_write_kv_continuous_fp8(to_dev(case.cos_sin), to_dev(case.end_lens),
+                                    to_dev(case.qkv), cache, qout,
+                                    torch.tensor([ks], dtype=torch.float32, device="cuda:0"),
+                                    torch.tensor([vs], dtype=torch.float32, device="cuda:0"),
+                                    Hq, Hkv, style)
+    torch.cuda.synchronize()
+    w_cache = case.new_cache8()
+    w_q = case.new_qout()
+    oracle.continuous_fp8(case.cos_sin, case.end_lens, case.qkv, w_cache, w_q, ks, vs, Hq, Hkv,
+                          style)
+    compare(to_host_bits(qout), w_q, qout_rotated(w_q.shape, r), f"{case.name} qOut")
+    compare_e4m3(cache.cpu().numpy(), w_cache, f"{case.name} cache")
