@@ -465,9 +465,10 @@ __global__ void __launch_bounds__(256) rope_kv_token_kernel(const TokenArgs a)
     // After the wait every load sees the previous grid's writes. The cos/sin
     // row of the speculative position is loaded now, in parallel with the
     // position itself; it is kept only if the position turns out the same.
-    // (Measured: 256 decode tokens 2.46 -> 2.38 us; the FP8 and normalized
-    // variants were slower with it, so they load after the position.)
-    if (!NORM && !FP8 && specPos >= 0 && rotItem)
+    // (Measured on 256 decode tokens: plain 2.46 -> 2.38 us, QK-normalized
+    // 2.58 -> 2.48 us; the FP8 variant was slower with it, 2.17 -> 2.38 us,
+    // so it loads after the position.)
+    if (!FP8 && specPos >= 0 && rotItem)
         load_cos_sin<STYLE, POL>(a.cosSin + ((size_t)bcRow * a.csSeq + specPos) * a.r, i, a.r, c,
                                  sn, pol);
 
@@ -503,7 +504,7 @@ __global__ void __launch_bounds__(256) rope_kv_token_kernel(const TokenArgs a)
 
     // 3. cos/sin for this thread's frequencies (unless the speculative
     // position's row, already loaded, is the right one)
-    if (rotItem && (NORM || FP8 || pos != specPos)) {
+    if (rotItem && (FP8 || pos != specPos)) {
         const float* row = a.cosSin + ((size_t)bcRow * a.csSeq + pos) * a.r;
         load_cos_sin<STYLE, POL>(row, i, a.r, c, sn, pol);
     }
