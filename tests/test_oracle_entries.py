@@ -311,3 +311,83 @@ def test_capacity_rule():
     assert not oracle.capacity_rejected(4000, 4096)
     assert oracle.capacity_rejected(4097, 4096)
     assert not oracle.capacity_rejected(0, 0)
+
+
+# ----------------------------------------------------- per-sequence tables --
+
+def batched_scale_table(B, rows, r):
+    """One table per sequence ("Apply Rope Write KV", cosSinCacheBatchSize = B):
+    sequence b's row k has cos 0 and sin 2^(k + 4b), so every rotated output
+    names both the row and the table it was read from."""
+    t = np.zeros((B, rows, r), dtype=np.float32)
+    for b in range(B):
+        for k in range(rows):
+            t[b, k, r // 2:] = 2.0 ** (k + 4 * b)
+    return t
+
+
+@pytest.mark.parametrize("mode", ["packed", "continuous", "tree"])
+@pytest.mark.parametrize("style", [oracle.NEOX, oracle.GPTJ])
+def test_per_sequence_tables(mode, style):
+    # B=2, S=2, Hq=2, Hkv=1, D=r=16, 4 rows per table. Codes stay <= 256 and
+    # scales <= 2^7, so every product is exact in FP16.
+    B, S, Hq, Hkv, D, r, cap = 2, 2, 2, 1, 16, 16, 4
+    qkv = coded_qkv(B, S, Hq + 2 * Hkv, D)
+    orig = qkv.copy()
+    cs = batched_scale_table(B, cap, r)
+    cache = workloads.sentinel_fill((B, 2, Hkv, cap, D))
+    qout = workloads.sentinel_fill((B, S, Hq, D))
+    end = np.array([2, 4], dtype=np.int32)           # b0 slots 0,1; b1 slots 2,3
+    if mode == "packed":
+        oracle.packed(cs, qkv, cache, Hq, Hkv, style)
+        pos = {(b, s): s for b in range(B) for s in range(S)}
+        slot = pos
+    elif mode == "continuous":
+        oracle.continuous(cs, end, qkv, cache, qout, Hq, Hkv, style)
+        pos = {(0, 0): 0, (0, 1): 1, (1, 0): 2, (1, 1): 3}
+        slot = pos
+    else:
+        ids = np.array([[1, 1], [0, 3]], dtype=np.int32)
+        oracle.tree(cs, end, ids, qkv, cache, qout, Hq, Hkv, style)
+        pos = {(0, 0): 1, (0, 1): 1, (1, 0): 0, (1, 1): 3}
+        slot = {(0, 0): 0, (0, 1): 1, (1, 0): 2, (1, 1): 3}
+    for (b, s), p in pos.items():
+        e = p + 4 * b                                   # table b, row p
+        qdst = qkv[b, s, :Hq] if mode == "packed" else qout[b, s]
+        for hq in range(Hq):
+            want = rotated_scaled(val(orig[b, s, hq]), r, style, e)
+            assert np.array_equal(val(qdst[hq]), want), (mode, b, s, hq)
+        want_k = rotated_scaled(val(orig[b, s, Hq]), r, style, e)
+        assert np.array_equal(val(cache[b, 0, 0, slot[(b, s)]]), want_k), (mode, b, s)
+        assert np.array_equal(cache[b, 1, 0, slot[(b, s)]], orig[b, s, Hq + 1])
+
+
+# ------------------------------------------- positions past the cos/sin table --
+
+def _table_prefix(rows, r, extra=1):
+    """A [1, rows, r] table that is the prefix of a larger array: a read of row
+    `rows` (one past the end) stays inside allocated memory and returns a row
+    of 2^10, which no pinned output may contain."""
+    big = np.zeros((1, rows + extra, r), dtype=np.float32)
+    big[0, :, : r // 2] = 1.0
+    big[0, rows:, :] = 2.0 ** 10
+    return big[:, :rows]
+
+
+@pytest.mark.parametrize("style", [oracle.NEOX, oracle.GPTJ])
+def test_tree_position_at_table_end_is_skipped(style):
+    # "Apply Rope Write KV", tree: the cos/sin row is tokenPosIds[b, s]; a
+    # position equal to cosSinSeqLen has no row, so the token writes nothing.
+    B, S, Hq, Hkv, D, r, cap = 1, 3, 2, 1, 16, 16, 8
+    qkv = coded_qkv(B, S, 4, D)
+    cs = _table_prefix(5, r)                          # rows 0..4
+    end = np.array([3], dtype=np.int32)               # slots 0, 1, 2
+    ids = np.array([[4, 5, 2]], dtype=np.int32)        # 5 == cosSinSeqLen
+    cache = workloads.sentinel_fill((B, 2, Hkv, cap, D))
+    qout = workloads.sentinel_fill((B, S, Hq, D))
+    oracle.tree(cs, end, ids, qkv, cache, qout, Hq, Hkv, style)
+    expect = {(0, 0, 0, 0): (0, 0, 2), (0, 1, 0, 0): (0, 0, 3),
+              (0, 0, 0, 2): (0, 2, 2), (0, 1, 0, 2): (0, 2, 3)}
+    _check_cache(cache, qkv, expect, {}, r, style, False)
+    assert np.all(qout[0, 1] == SENT)
+    assert np.array_equal(qout[0, 0], qkv[0, 0, :2]) and np.array_equal(qout[0, 2], qkv[0, 2, :2])

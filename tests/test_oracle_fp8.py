@@ -122,3 +122,21 @@ def test_fp8_cache_scaled_rotation_closed_form():
     assert c8[0, 0, 0, 1, 0] == oracle.f64_to_e4m3(c1 / 0.25)
     assert c8[0, 0, 0, 1, r // 2] == oracle.f64_to_e4m3(s1 / 0.25)
     assert abs(oracle.e4m3_to_f64(c8[0, 0, 0, 1, 0]) - math.cos(1.0) * 4) <= 0.0625 * 2
+
+
+def test_fp8_position_past_table_is_skipped():
+    # slots and positions as the continuous call: position 5 of a 5-row table
+    # has no cos/sin row, so that token writes neither qOut nor the FP8 cache
+    B, S, Hq, Hkv, D, r, cap = 1, 3, 2, 1, 16, 16, 8
+    qkv = np.full((B, S, 4, D), 0.5).astype(np.float16).view(np.uint16)
+    big = np.zeros((1, 6, r), dtype=np.float32)
+    big[0, :, : r // 2] = 1.0
+    big[0, 5] = 2.0 ** 10                                 # one row past the table
+    cs = big[:, :5]
+    end = np.array([6], dtype=np.int32)                   # positions 3, 4, 5
+    c8 = np.full((B, 2, Hkv, cap, D), 0x7F, dtype=np.uint8)
+    q8 = workloads.sentinel_fill((B, S, Hq, D))
+    oracle.continuous_fp8(cs, end, qkv, c8, q8, 1.0, 1.0, Hq, Hkv, oracle.NEOX)
+    assert np.all(q8[0, 2] == workloads.SENTINEL) and np.all(c8[0, :, 0, 5] == 0x7F)
+    assert np.all(c8[0, :, 0, 3:5] == oracle.f64_to_e4m3(0.5))
+    assert np.all(c8[0, :, 0, :3] == 0x7F) and np.all(c8[0, :, 0, 6:] == 0x7F)

@@ -75,6 +75,17 @@ MUTANTS = {
     "fp8_scale_not_inverted": ("kc[d] = ropekv_oracle_f64_to_e4m3(y[d] * (1.0 / (double)kScale));",
                                "kc[d] = ropekv_oracle_f64_to_e4m3(y[d] * (double)kScale);"),
     "slotmap_stride_ignored": ("rope_head_f16(k + (size_t)t * kStride", "rope_head_f16(k + (size_t)t * Hkv * D"),
+    "cs_batch_ignored": ("int bc = (csBatch == 1) ? 0 : b;", "int bc = 0;"),
+    "qknorm_tail_copied": ("for (int d = 0; d < D; ++d)\n        dst[d] = ropekv_oracle_f64_to_f16(y[d]);",
+                           "for (int d = 0; d < D; ++d)\n        dst[d] = (d < r) ? ropekv_oracle_f64_to_f16(y[d]) : src[d];"),
+    "qknorm_after_rotation": ("ropekv_oracle_rms_norm_f64(x, weight, eps, D, n);\n    ropekv_oracle_rope_head_f64(n, cs, D, r, style, y);",
+                              "ropekv_oracle_rope_head_f64(x, cs, D, r, style, n);\n    ropekv_oracle_rms_norm_f64(n, weight, eps, D, y);"),
+    "qknorm_pos_upper_unchecked": ("long long slot = pos;\n            if (slot < 0 || slot >= cap || pos >= csSeq)",
+                                   "long long slot = pos;\n            if (slot < 0 || slot >= cap)"),
+    "tree_pos_upper_unchecked": ("if (pos < 0 || pos >= csSeq || slot < 0 || slot >= cap)",
+                                 "if (pos < 0 || slot < 0 || slot >= cap)"),
+    "fp8_pos_upper_unchecked": ("if (slot < 0 || slot >= cap || slot >= csSeq)",
+                                "if (slot < 0 || slot >= cap)"),
 }
 
 

@@ -81,3 +81,61 @@ def test_q_and_k_use_their_own_weights_and_v_is_copied():
     assert np.all(qo.view(np.float16) == 0.5)
     assert np.all(cache[0, 0, 0, 0].view(np.float16) == 4.0)
     assert np.array_equal(cache[0, 1, 0, 0], qkv[0, 0, 3])
+
+
+@pytest.mark.parametrize("style", [oracle.NEOX, oracle.GPTJ])
+def test_partial_rotary_tail_is_normalized_with_weights(style):
+    """Constant heads c with eps 0 normalize to sign(c) * w exactly. With
+    r < D and weights that differ per dim, dims past rotaryDim must hold
+    fp16(sign(c) * w[d]) -- normalized, not the input bits -- and rotated dims
+    must be rotate(sign(c) * w) * 2^p for a "scale" row p (cos 0, sin 2^p):
+    the weight is applied before the rotation, on the head's own dims."""
+    B, S, Hq, Hkv, D, r, cap = 1, 2, 2, 1, 64, 32, 4
+    consts = {(0, 0): 3.0, (0, 1): -0.25, (0, 2): 0.5, (1, 0): -2.0, (1, 1): 1.0, (1, 2): 4.0}
+    qkv = np.zeros((B, S, Hq + 2 * Hkv, D), dtype=np.float64)
+    for (s, h), c in consts.items():
+        qkv[0, s, h] = c
+    qkv[0, :, 3] = np.arange(D) / 8.0                     # V heads: copied as bits
+    qkv = qkv.astype(np.float16).view(np.uint16)
+    wq = 1.0 + np.arange(D) / 64.0                        # exact in FP16
+    wk = 2.0 - np.arange(D) / 128.0
+    cs = np.zeros((1, cap, r), dtype=np.float32)
+    for p in range(cap):
+        cs[0, p, r // 2:] = 2.0 ** p
+    end = np.array([3], dtype=np.int32)                   # positions 1, 2
+    cache = workloads.sentinel_fill((B, 2, Hkv, cap, D))
+    qo = workloads.sentinel_fill((B, S, Hq, D))
+    oracle.continuous_qknorm(cs, end, qkv, cache, qo, _w(wq), _w(wk), 0.0, Hq, Hkv, style)
+    h = r // 2
+    for s in range(S):
+        p = s + 1
+        for head in range(3):
+            w = wq if head < Hq else wk
+            n = np.sign(consts[(s, head)]) * w
+            want = n.copy()
+            for d in range(r):
+                if style == oracle.NEOX:
+                    want[d] = (-n[d + h] if d < h else n[d - h]) * 2.0 ** p
+                else:
+                    want[d] = (-n[d + 1] if d % 2 == 0 else n[d - 1]) * 2.0 ** p
+            got = qo[0, s, head] if head < Hq else cache[0, 0, 0, p]
+            assert np.array_equal(got.view(np.float16).astype(np.float64), want), (s, head)
+        assert np.array_equal(cache[0, 1, 0, p], qkv[0, s, 3])
+
+
+def test_qknorm_position_past_table_is_skipped():
+    # as the continuous call: a slot/position >= cosSinSeqLen writes nothing
+    B, S, Hq, Hkv, D, r, cap = 1, 3, 2, 1, 64, 64, 8
+    qkv = np.ones((B, S, 4, D)).astype(np.float16).view(np.uint16)
+    big = np.zeros((1, 6, r), dtype=np.float32)
+    big[0, :, : r // 2] = 1.0
+    big[0, 5] = 2.0 ** 10                                 # one row past the table
+    cs = big[:, :5]
+    end = np.array([6], dtype=np.int32)                   # positions 3, 4, 5
+    cache = workloads.sentinel_fill((B, 2, Hkv, cap, D))
+    qo = workloads.sentinel_fill((B, S, Hq, D))
+    ones = _w(np.ones(D))
+    oracle.continuous_qknorm(cs, end, qkv, cache, qo, ones, ones, 0.0, Hq, Hkv, oracle.NEOX)
+    assert np.all(qo[0, 2] == workloads.SENTINEL) and np.all(cache[0, :, 0, 5] == workloads.SENTINEL)
+    assert np.all(qo[0, :2].view(np.float16) == 1.0)
+    assert np.all(cache[0, 0, 0, 3:5].view(np.float16) == 1.0)
