@@ -27,17 +27,26 @@
  *     16-byte aligned. The library allocates nothing and never synchronises;
  *     results are ready when the stream says so. Its only state is a record,
  *     per kernel and device, that the kernel's dynamic shared memory limit was
- *     raised: decode-sized launches (fewer than 1024 tokens) reserve shared
- *     memory they do not use so that their CTAs spread over all SMs.
+ *     raised, and the residency-cap switch (ropekv_set_residency_cap):
+ *     decode-sized launches (fewer than 1024 tokens) reserve shared memory
+ *     they do not use so that their CTAs spread over all SMs.
  *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *     stream). Calls are asynchronous and may be captured in a CUDA graph.
+ *     The calling thread's current CUDA device must be the device that holds
+ *     the tensors and the stream (as for any kernel launch): the launch and
+ *     the residency cap use the current device.
  *   - cos/sin rows hold rotaryDim floats: cos_0..cos_{r/2-1} then
  *     sin_0..sin_{r/2-1} ([RC] _load_cos_sin and the half-width table rule).
  *     Dims i and partner use frequency i: NeoX pairs (i, i + r/2), GPT-J pairs
  *     (2i, 2i + 1) ([RC] rotate layouts and Stage 2.1). Dims >= rotaryDim and
  *     all V heads are copied bit for bit.
  *   - Return value: ROPEKV_OK (0), or a negative ropekv_status when the host
- *     rejected the arguments (nothing launched) or the launch failed.
+ *     rejected the arguments (nothing launched) or the launch failed. A
+ *     launch failure is read from that launch's own result
+ *     (cudaLaunchKernelEx); the library never calls cudaGetLastError on a
+ *     launch path, so it neither reports nor clears an error that the caller
+ *     left pending. (An error that earlier work left in the context can still
+ *     make the launch itself fail.)
  *     Data-dependent invalid indices found on the device (negative or
  *     out-of-range positions, sequences, slots or pages) are skipped: nothing
  *     is written for them, and no error is raised ([DRK] skip rules).
@@ -255,6 +264,8 @@ ROPEKV_API int rope_write_kv_slot_mapping(const float* cosSin, const int64_t* po
  *                          j >= deltaLengths[b] are padding.
  *   stateIndices           [batchSize] INT32 source row of each sequence, or NULL
  *                          (then row 0 when sourceRows == 1, else row b).
+ *   cosSinSource may be NULL when sourceRows == 0 (as for the gather): every
+ *   row's cos/sin is then zero.
  * Token j of sequence b sits at position oldDraftCacheLengths[b] + j. When its
  * position is >= cacheCapacity or its source row is outside [0, sourceRows) the
  * gather yields a zero cos/sin row, so rotated K dims are written as zeros.
@@ -317,6 +328,26 @@ ROPEKV_API int dflash_gather_delta_rope(const float* source, float* output,
  * ROPEKV_ERR_CAPACITY (the page's version throws instead).
  */
 ROPEKV_API int rope_check_capacity(int32_t cosSinSeqLen, int32_t kvCapacity);
+
+/*
+ * Process-wide switch of the residency cap of decode-sized launches (fewer
+ * than 1024 tokens or rows): 1 (the default) = on, 0 = off. Returns the
+ * previous setting. Thread-safe; takes effect for launches made after it.
+ *
+ * With the cap on, a decode-sized launch reserves dynamic shared memory that
+ * its kernel does not use, sized so that at most ceil(grid / SMs) of its CTAs
+ * fit on one SM. A launch that starts while its predecessor in the stream
+ * still runs (programmatic dependent launch) otherwise has its CTAs packed
+ * onto a minority of the SMs, and it lasts as long as the busiest SM (on
+ * GB300, 256 decode tokens: 2.40 us uncapped, about 2.1 us capped). The cost
+ * falls on concurrent work: while a kernel on another stream holds shared
+ * memory on an SM, a capped CTA may not fit there and waits for another SM,
+ * and the capped CTAs in turn keep other kernels' shared-memory-hungry CTAs
+ * off the SMs they occupy. A caller that overlaps these writes with
+ * shared-memory-heavy kernels (attention, GEMMs) can switch the cap off.
+ * Results are identical either way. (Not in the pages: a launch-shape choice.)
+ */
+ROPEKV_API int ropekv_set_residency_cap(int enable);
 
 /* Static, human-readable text for a status code (never NULL). */
 ROPEKV_API const char* ropekv_status_string(int status);

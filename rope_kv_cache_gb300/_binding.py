@@ -69,6 +69,8 @@ def load_library():
     lib.rope_write_kv_slot_mapping.argtypes = [P, P, P, I64, P, I64, P, I64, P, P, P, P, P,
                                                I32, I32, I32, I32, I32, I32, I64, I32, I32, P]
     lib.rope_check_capacity.argtypes = [I32, I32]
+    lib.ropekv_set_residency_cap.argtypes = [ctypes.c_int]
+    lib.ropekv_set_residency_cap.restype = ctypes.c_int
     lib.ropekv_status_string.argtypes = [ctypes.c_int]
     lib.ropekv_status_string.restype = ctypes.c_char_p
     for fn in ("rope_write_kv_packed", "rope_write_kv_continuous", "rope_write_kv_tree",
@@ -79,6 +81,31 @@ def load_library():
         getattr(lib, fn).restype = ctypes.c_int
     _lib = lib
     return lib
+
+
+class _on:
+    """The library's entry points, each called with ``device`` made the
+    calling thread's current CUDA device for the duration of the call: a
+    launch, and the residency cap of small launches, act on the current
+    device, which need not be the one holding the tensors."""
+
+    def __init__(self, device):
+        self._device = device
+
+    def __getattr__(self, name):
+        fn = getattr(load_library(), name)
+
+        def call(*args):
+            with torch.cuda.device(self._device):
+                return fn(*args)
+        return call
+
+
+def ropekv_set_residency_cap(enable: bool) -> bool:
+    """Switch the residency cap of decode-sized launches on (default) or off,
+    process-wide; returns the previous setting. Results are identical either
+    way; see include/ropekv.h for what the cap costs concurrent kernels."""
+    return bool(load_library().ropekv_set_residency_cap(1 if enable else 0))
 
 
 def ropekv_status_string(status: int) -> str:
@@ -166,7 +193,7 @@ def rope_write_kv_packed(cos_sin: torch.Tensor, qkv: torch.Tensor, kv_cache: tor
     """
     dims = _contiguous_dims(cos_sin, qkv, kv_cache, num_q_heads, num_kv_heads, style)
     dev = qkv.device
-    rc = load_library().rope_write_kv_packed(
+    rc = _on(dev).rope_write_kv_packed(
         _dev_ptr(cos_sin, "cos_sin", _F32, dev), _dev_ptr(qkv, "qkv", _F16, dev),
         _dev_ptr(kv_cache, "kv_cache", _F16, dev), ctypes.byref(dims), _stream_handle(stream, dev))
     _check_rc("rope_write_kv_packed", rc)
@@ -183,7 +210,7 @@ def rope_write_kv_continuous(cos_sin: torch.Tensor, kv_cache_end_lens: torch.Ten
     if tuple(kv_cache_end_lens.shape) != (B,) or tuple(q_out.shape) != (B, S, num_q_heads, D):
         raise ValueError("kv_cache_end_lens [B] and q_out [B,S,Hq,D] expected")
     dev = qkv.device
-    rc = load_library().rope_write_kv_continuous(
+    rc = _on(dev).rope_write_kv_continuous(
         _dev_ptr(cos_sin, "cos_sin", _F32, dev),
         _dev_ptr(kv_cache_end_lens, "kv_cache_end_lens", _I32, dev),
         _dev_ptr(qkv, "qkv", _F16, dev), _dev_ptr(kv_cache, "kv_cache", _F16, dev),
@@ -205,7 +232,7 @@ def rope_write_kv_continuous_qknorm(cos_sin: torch.Tensor, kv_cache_end_lens: to
             or tuple(q_norm_weight.shape) != (D,) or tuple(k_norm_weight.shape) != (D,):
         raise ValueError("kv_cache_end_lens [B], q_out [B,S,Hq,D], norm weights [D] expected")
     dev = qkv.device
-    rc = load_library().rope_write_kv_continuous_qknorm(
+    rc = _on(dev).rope_write_kv_continuous_qknorm(
         _dev_ptr(cos_sin, "cos_sin", _F32, dev),
         _dev_ptr(kv_cache_end_lens, "kv_cache_end_lens", _I32, dev),
         _dev_ptr(qkv, "qkv", _F16, dev), _dev_ptr(kv_cache, "kv_cache", _F16, dev),
@@ -231,7 +258,7 @@ def rope_write_kv_continuous_fp8(cos_sin: torch.Tensor, kv_cache_end_lens: torch
             or k_scale.numel() != 1 or v_scale.numel() != 1:
         raise ValueError("kv_cache_end_lens [B], q_out [B,S,Hq,D], one-element scales expected")
     dev = qkv.device
-    rc = load_library().rope_write_kv_continuous_fp8(
+    rc = _on(dev).rope_write_kv_continuous_fp8(
         _dev_ptr(cos_sin, "cos_sin", _F32, dev),
         _dev_ptr(kv_cache_end_lens, "kv_cache_end_lens", _I32, dev),
         _dev_ptr(qkv, "qkv", _F16, dev), _dev_ptr(kv_cache, "kv_cache", _U8, dev),
@@ -252,7 +279,7 @@ def rope_write_kv_tree(cos_sin: torch.Tensor, kv_cache_end_lens: torch.Tensor,
             or tuple(q_out.shape) != (B, S, num_q_heads, D):
         raise ValueError("kv_cache_end_lens [B], token_pos_ids [B,S], q_out [B,S,Hq,D] expected")
     dev = qkv.device
-    rc = load_library().rope_write_kv_tree(
+    rc = _on(dev).rope_write_kv_tree(
         _dev_ptr(cos_sin, "cos_sin", _F32, dev),
         _dev_ptr(kv_cache_end_lens, "kv_cache_end_lens", _I32, dev),
         _dev_ptr(token_pos_ids, "token_pos_ids", _I32, dev),
@@ -286,7 +313,7 @@ def paged_kv_delta_update(k_delta: torch.Tensor, v_delta: torch.Tensor, kv_cache
     if batch_size > B:
         raise ValueError("batch_size exceeds the page table's rows")
     dev = k_delta.device
-    rc = load_library().paged_kv_delta_update(
+    rc = _on(dev).paged_kv_delta_update(
         _dev_ptr(k_delta, "k_delta", _F16, dev), _dev_ptr(v_delta, "v_delta", _F16, dev),
         _dev_ptr(kv_cache, "kv_cache", _F16, dev),
         _dev_ptr(token_aligned_cos_sin, "token_aligned_cos_sin", _F32, dev),
@@ -327,7 +354,7 @@ def paged_kv_delta_update_fused(k_delta: torch.Tensor, v_delta: torch.Tensor,
             or (state_indices is not None and tuple(state_indices.shape) != (B,)):
         raise ValueError("inconsistent shapes for paged_kv_delta_update_fused")
     dev = k_delta.device
-    rc = load_library().paged_kv_delta_update_fused(
+    rc = _on(dev).paged_kv_delta_update_fused(
         _dev_ptr(k_delta, "k_delta", _F16, dev), _dev_ptr(v_delta, "v_delta", _F16, dev),
         _dev_ptr(kv_cache, "kv_cache", _F16, dev),
         _dev_ptr(cos_sin_source, "cos_sin_source", _F32, dev),
@@ -351,7 +378,7 @@ def dflash_prepare_delta_metadata(old_draft_cache_lengths: torch.Tensor,
             or delta_token_to_sequence.numel() != B * delta_width:
         raise ValueError("inconsistent shapes for dflash_prepare_delta_metadata")
     dev = old_draft_cache_lengths.device
-    rc = load_library().dflash_prepare_delta_metadata(
+    rc = _on(dev).dflash_prepare_delta_metadata(
         _dev_ptr(old_draft_cache_lengths, "old_draft_cache_lengths", _I32, dev),
         _dev_ptr(delta_lengths, "delta_lengths", _I32, dev), int(delta_width),
         _dev_ptr(delta_positions, "delta_positions", _I32, dev),
@@ -377,7 +404,7 @@ def dflash_gather_delta_rope(source: torch.Tensor, output: torch.Tensor,
     if batch_size is None:
         batch_size = state_indices.shape[0] if state_indices is not None else N
     dev = output.device
-    rc = load_library().dflash_gather_delta_rope(
+    rc = _on(dev).dflash_gather_delta_rope(
         _dev_ptr(source, "source", _F32, dev), _dev_ptr(output, "output", _F32, dev),
         _dev_ptr(delta_positions, "delta_positions", _I32, dev),
         _dev_ptr(delta_token_to_sequence, "delta_token_to_sequence", _I32, dev),
@@ -409,7 +436,7 @@ def rope_write_kv_slot_mapping(cos_sin: torch.Tensor, positions: torch.Tensor, q
     qp, qs = _dev_rows(q, "q", dev)
     kp, ks = _dev_rows(k, "k", dev)
     vp, vs = _dev_rows(v, "v", dev)
-    rc = load_library().rope_write_kv_slot_mapping(
+    rc = _on(dev).rope_write_kv_slot_mapping(
         _dev_ptr(cos_sin, "cos_sin", _F32, dev), _dev_ptr(positions, "positions", _I64, dev),
         qp, qs, kp, ks, vp, vs, _dev_ptr(slot_mapping, "slot_mapping", _I64, dev),
         _dev_ptr(key_cache, "key_cache", _F16, dev), _dev_ptr(value_cache, "value_cache", _F16, dev),

@@ -3,7 +3,9 @@
 // the caller's stream. Declarations and the meaning of every argument are in
 // include/ropekv.h. Nothing here allocates or synchronises; the only state is
 // a per-kernel record of the devices on which its dynamic shared memory limit
-// was raised (see residency_smem).
+// was raised (see residency_smem) and the process-wide residency-cap switch.
+// Every entry point returns the status of its own launch: the library never
+// reads or clears CUDA's per-thread "last error" for the caller.
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -20,11 +22,6 @@ using ropekv::TokenArgs;
 bool aligned16(const void* p)
 {
     return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
-}
-
-int launch_status()
-{
-    return cudaGetLastError() == cudaSuccess ? ROPEKV_OK : ROPEKV_ERR_LAUNCH;
 }
 
 int check_head_dims(int32_t D, int32_t r)
@@ -110,9 +107,12 @@ bool pdl_allowed(unsigned grid, const Shape& sh)
     return grid <= kPdlMaxCtas || sh.threads * sh.ipt >= 256;
 }
 
+// One launch; returns ROPEKV_OK or ROPEKV_ERR_LAUNCH from this launch's own
+// result (cudaLaunchKernelEx reports configuration errors of this launch; an
+// error left pending by earlier work in the context may also surface here).
 template <typename Args>
-void launch_k(void (*kern)(Args), unsigned grid, int threads, cudaStream_t st, bool pdl,
-              const Args& a, size_t smem = 0)
+int launch_k(void (*kern)(Args), unsigned grid, int threads, cudaStream_t st, bool pdl,
+             const Args& a, size_t smem = 0)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
@@ -124,8 +124,11 @@ void launch_k(void (*kern)(Args), unsigned grid, int threads, cudaStream_t st, b
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = pdl ? attr : nullptr;
     cfg.numAttrs = pdl ? 1 : 0;
-    (void)cudaLaunchKernelEx(&cfg, kern, a);
+    return cudaLaunchKernelEx(&cfg, kern, a) == cudaSuccess ? ROPEKV_OK : ROPEKV_ERR_LAUNCH;
 }
+
+// Process-wide switch of the residency cap below (ropekv_set_residency_cap).
+std::atomic<int> g_residency_cap{1};
 
 // Residency cap of a small dependent launch. A launch that starts while its
 // predecessor still runs gets its CTAs placed densely: a per-warp timer trace
@@ -134,12 +137,16 @@ void launch_k(void (*kern)(Args), unsigned grid, int threads, cudaStream_t st, b
 // issue their work. Dynamic shared memory that the kernel does not use, sized
 // so that at most ceil(grid / SMs) CTAs fit on one SM, spreads the CTAs over
 // the GPU (256 decode tokens: 2.40 -> 2.07 us per launch). Returns 0 (no cap)
-// for grids of more than 8 CTAs per SM or when the device cannot be queried;
+// for grids of more than 8 CTAs per SM, when the caller switched the cap off
+// or when the device cannot be queried (a failed query's error is consumed
+// here: it is this function's own, and the launch then goes ahead uncapped);
 // *optin receives the device's per-block shared memory limit.
 size_t residency_smem(unsigned grid, int* optin)
 {
     int dev = 0, sms = 0, perSm = 0, reserved = 0;
     *optin = 0;
+    if (!g_residency_cap.load(std::memory_order_relaxed))
+        return 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&perSm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) !=
@@ -165,7 +172,7 @@ size_t residency_smem(unsigned grid, int* optin)
 // device's maximum once per device (one bit per device ordinal below 64;
 // higher ordinals raise it on every call) -- the only state the library keeps.
 template <auto Kern, typename Args>
-void launch_small(unsigned grid, int threads, cudaStream_t st, const Args& a)
+int launch_small(unsigned grid, int threads, cudaStream_t st, const Args& a)
 {
     int optin = 0;
     size_t smem = residency_smem(grid, &optin);
@@ -179,110 +186,103 @@ void launch_small(unsigned grid, int threads, cudaStream_t st, const Args& a)
                 cudaSuccess) {
                 raised.fetch_or(bit, std::memory_order_relaxed);
             } else {
-                (void)cudaGetLastError();
+                (void)cudaGetLastError();  // this call's own error, handled here
                 smem = 0;  // launch without the cap rather than fail
             }
         }
     }
-    launch_k(Kern, grid, threads, st, true, a, smem);
+    return launch_k(Kern, grid, threads, st, true, a, smem);
 }
 
 template <int D, int STYLE, int MODE, int IPT, bool NORM, bool FP8>
-void launch_token_variant(const TokenArgs& a, unsigned grid, const Shape& sh, cudaStream_t st)
+int launch_token_variant(const TokenArgs& a, unsigned grid, const Shape& sh, cudaStream_t st)
 {
     if constexpr (IPT == 2) {
-        if (sh.small) {
-            launch_small<ropekv::rope_kv_token_kernel<D, STYLE, MODE, IPT, kPolSmall, NORM, FP8>>(
+        if (sh.small)
+            return launch_small<
+                ropekv::rope_kv_token_kernel<D, STYLE, MODE, IPT, kPolSmall, NORM, FP8>>(
                 grid, sh.threads, st, a);
-            return;
-        }
     }
     if (pdl_allowed(grid, sh))
-        launch_k(ropekv::rope_kv_token_kernel<D, STYLE, MODE, IPT, kPolPdl, NORM, FP8>, grid,
-                 sh.threads, st, true, a);
-    else
-        launch_k(ropekv::rope_kv_token_kernel<D, STYLE, MODE, IPT, kPolLarge, NORM, FP8>, grid,
-                 sh.threads, st, false, a);
+        return launch_k(ropekv::rope_kv_token_kernel<D, STYLE, MODE, IPT, kPolPdl, NORM, FP8>,
+                        grid, sh.threads, st, true, a);
+    return launch_k(ropekv::rope_kv_token_kernel<D, STYLE, MODE, IPT, kPolLarge, NORM, FP8>, grid,
+                    sh.threads, st, false, a);
 }
 
 template <int D, int STYLE, int MODE, int IPT>
-void launch_token(const TokenArgs& a, long long tokens, const Shape& sh, cudaStream_t st)
+int launch_token(const TokenArgs& a, long long tokens, const Shape& sh, cudaStream_t st)
 {
     const unsigned grid = (unsigned)(tokens * sh.ctasPerUnit);
     if constexpr (MODE == ropekv::kContinuous) {
-        if (a.qNormW != nullptr) {
-            launch_token_variant<D, STYLE, MODE, IPT, true, false>(a, grid, sh, st);
-            return;
-        }
+        if (a.qNormW != nullptr)
+            return launch_token_variant<D, STYLE, MODE, IPT, true, false>(a, grid, sh, st);
         if (a.cache8 != nullptr) {
             if constexpr (IPT != 4)
-                launch_token_variant<D, STYLE, MODE, IPT, false, true>(a, grid, sh, st);
-            return;
+                return launch_token_variant<D, STYLE, MODE, IPT, false, true>(a, grid, sh, st);
+            return ROPEKV_ERR_LAUNCH;  // pick_shape never gives the FP8 call 4 items
         }
     }
     if constexpr (IPT != 4)
-        launch_token_variant<D, STYLE, MODE, IPT, false, false>(a, grid, sh, st);
+        return launch_token_variant<D, STYLE, MODE, IPT, false, false>(a, grid, sh, st);
+    return ROPEKV_ERR_LAUNCH;  // 4 items per thread: the normalized call only
 }
 
 template <int D, int STYLE, int MODE>
-void dispatch_ipt(const TokenArgs& a, long long tokens, const Shape& sh, cudaStream_t st)
+int dispatch_ipt(const TokenArgs& a, long long tokens, const Shape& sh, cudaStream_t st)
 {
     if (sh.ipt == 4) {
         if constexpr (MODE == ropekv::kContinuous)
-            launch_token<D, STYLE, MODE, 4>(a, tokens, sh, st);  // the normalized call only
-    } else {
-        launch_token<D, STYLE, MODE, 2>(a, tokens, sh, st);
+            return launch_token<D, STYLE, MODE, 4>(a, tokens, sh, st);  // the normalized call only
+        return ROPEKV_ERR_LAUNCH;
     }
+    return launch_token<D, STYLE, MODE, 2>(a, tokens, sh, st);
 }
 
 template <int D, int MODE>
-void dispatch_style(const TokenArgs& a, int style, long long tokens, const Shape& sh,
-                    cudaStream_t st)
+int dispatch_style(const TokenArgs& a, int style, long long tokens, const Shape& sh,
+                   cudaStream_t st)
 {
     if (style == ROPEKV_GPTJ)
-        dispatch_ipt<D, ropekv::kGptj, MODE>(a, tokens, sh, st);
-    else
-        dispatch_ipt<D, ropekv::kNeox, MODE>(a, tokens, sh, st);
+        return dispatch_ipt<D, ropekv::kGptj, MODE>(a, tokens, sh, st);
+    return dispatch_ipt<D, ropekv::kNeox, MODE>(a, tokens, sh, st);
 }
 
 template <int MODE>
-void dispatch_token(const TokenArgs& a, int D, int style, long long tokens, const Shape& sh,
-                    cudaStream_t st)
+int dispatch_token(const TokenArgs& a, int D, int style, long long tokens, const Shape& sh,
+                   cudaStream_t st)
 {
     switch (D) {
-    case 64: dispatch_style<64, MODE>(a, style, tokens, sh, st); break;
-    case 128: dispatch_style<128, MODE>(a, style, tokens, sh, st); break;
-    default: dispatch_style<256, MODE>(a, style, tokens, sh, st); break;
+    case 64: return dispatch_style<64, MODE>(a, style, tokens, sh, st);
+    case 128: return dispatch_style<128, MODE>(a, style, tokens, sh, st);
+    default: return dispatch_style<256, MODE>(a, style, tokens, sh, st);
     }
 }
 
 template <int D, int STYLE, bool FUSED>
-void launch_paged(const PagedArgs& a, long long rows, const Shape& sh, cudaStream_t st)
+int launch_paged(const PagedArgs& a, long long rows, const Shape& sh, cudaStream_t st)
 {
     // pick_shape gives the paged rows (never "heavy") two items per thread
     const unsigned grid = (unsigned)(rows * sh.ctasPerUnit);
-    launch_k(ropekv::paged_delta_kernel<D, STYLE, 2, kPolLarge, FUSED>, grid, sh.threads, st,
-             false, a);
+    return launch_k(ropekv::paged_delta_kernel<D, STYLE, 2, kPolLarge, FUSED>, grid, sh.threads,
+                    st, false, a);
 }
 
 template <bool FUSED>
-void dispatch_paged(const PagedArgs& a, int D, int style, long long rows, const Shape& sh,
-                    cudaStream_t st)
+int dispatch_paged(const PagedArgs& a, int D, int style, long long rows, const Shape& sh,
+                   cudaStream_t st)
 {
     const bool gptj = style == ROPEKV_GPTJ;
     switch (D) {
     case 64:
-        gptj ? launch_paged<64, ropekv::kGptj, FUSED>(a, rows, sh, st)
-             : launch_paged<64, ropekv::kNeox, FUSED>(a, rows, sh, st);
-        break;
+        return gptj ? launch_paged<64, ropekv::kGptj, FUSED>(a, rows, sh, st)
+                    : launch_paged<64, ropekv::kNeox, FUSED>(a, rows, sh, st);
     case 128:
-        gptj ? launch_paged<128, ropekv::kGptj, FUSED>(a, rows, sh, st)
-             : launch_paged<128, ropekv::kNeox, FUSED>(a, rows, sh, st);
-        break;
+        return gptj ? launch_paged<128, ropekv::kGptj, FUSED>(a, rows, sh, st)
+                    : launch_paged<128, ropekv::kNeox, FUSED>(a, rows, sh, st);
     default:
-        gptj ? launch_paged<256, ropekv::kGptj, FUSED>(a, rows, sh, st)
-             : launch_paged<256, ropekv::kNeox, FUSED>(a, rows, sh, st);
-        break;
+        return gptj ? launch_paged<256, ropekv::kGptj, FUSED>(a, rows, sh, st)
+                    : launch_paged<256, ropekv::kNeox, FUSED>(a, rows, sh, st);
     }
 }
 
@@ -311,11 +311,8 @@ int launch_paged_rows(PagedArgs& a, long long rows, int D, int style, bool fused
     if (rows * sh.ctasPerUnit > 0x7FFFFFFFLL)
         return ROPEKV_ERR_SHAPE;
     a.ctasPerRow = sh.ctasPerUnit;
-    if (fused)
-        dispatch_paged<true>(a, D, style, rows, sh, st);
-    else
-        dispatch_paged<false>(a, D, style, rows, sh, st);
-    return launch_status();
+    return fused ? dispatch_paged<true>(a, D, style, rows, sh, st)
+                 : dispatch_paged<false>(a, D, style, rows, sh, st);
 }
 
 // Checks shared by the three contiguous-cache calls. On success fills the
@@ -368,16 +365,33 @@ int launch_contiguous(TokenArgs a, const ropekv_dims* d, long long tokens, int m
     a.ctasPerToken = sh.ctasPerUnit;
     switch (mode) {
     case ropekv::kPacked:
-        dispatch_token<ropekv::kPacked>(a, d->headDim, d->style, tokens, sh, st);
-        break;
+        return dispatch_token<ropekv::kPacked>(a, d->headDim, d->style, tokens, sh, st);
     case ropekv::kContinuous:
-        dispatch_token<ropekv::kContinuous>(a, d->headDim, d->style, tokens, sh, st);
-        break;
+        return dispatch_token<ropekv::kContinuous>(a, d->headDim, d->style, tokens, sh, st);
     default:
-        dispatch_token<ropekv::kTree>(a, d->headDim, d->style, tokens, sh, st);
-        break;
+        return dispatch_token<ropekv::kTree>(a, d->headDim, d->style, tokens, sh, st);
     }
-    return launch_status();
+}
+
+template <int D>
+int launch_slotmap(const ropekv::SlotMapArgs& a, bool gptj, unsigned grid, const Shape& sh,
+                   cudaStream_t st)
+{
+    using ropekv::rope_kv_slotmap_kernel;
+    if (sh.small)
+        return gptj ? launch_small<rope_kv_slotmap_kernel<D, ropekv::kGptj, 2, kPolSmall>>(
+                          grid, sh.threads, st, a)
+                    : launch_small<rope_kv_slotmap_kernel<D, ropekv::kNeox, 2, kPolSmall>>(
+                          grid, sh.threads, st, a);
+    if (pdl_allowed(grid, sh))
+        return gptj ? launch_k(rope_kv_slotmap_kernel<D, ropekv::kGptj, 2, kPolPdl>, grid,
+                               sh.threads, st, true, a)
+                    : launch_k(rope_kv_slotmap_kernel<D, ropekv::kNeox, 2, kPolPdl>, grid,
+                               sh.threads, st, true, a);
+    return gptj ? launch_k(rope_kv_slotmap_kernel<D, ropekv::kGptj, 2, kPolLarge>, grid,
+                           sh.threads, st, false, a)
+                : launch_k(rope_kv_slotmap_kernel<D, ropekv::kNeox, 2, kPolLarge>, grid,
+                           sh.threads, st, false, a);
 }
 
 }  // namespace
@@ -576,8 +590,10 @@ int paged_kv_delta_update_fused(const uint16_t* kDelta, const uint16_t* vDelta,
         return rc;
     if (rows == 0)
         return ROPEKV_OK;
-    if (!kDelta || !vDelta || !kvCache || !cosSinSource || !oldDraftCacheLengths ||
-        !deltaLengths || !pageTable)
+    // as the gather: without source rows there is nothing to read, and every
+    // rotated K dim is written as zero
+    if (!kDelta || !vDelta || !kvCache || (!cosSinSource && sourceRows > 0) ||
+        !oldDraftCacheLengths || !deltaLengths || !pageTable)
         return ROPEKV_ERR_NULL_POINTER;
     if (!aligned16(kDelta) || !aligned16(vDelta) || !aligned16(kvCache) ||
         !aligned16(cosSinSource) || !aligned16(oldDraftCacheLengths) ||
@@ -625,8 +641,7 @@ int dflash_prepare_delta_metadata(const int32_t* oldDraftCacheLengths,
     ropekv::DeltaMetaArgs a = {oldDraftCacheLengths, deltaLengths, deltaPositions,
                                deltaTokenToSequence, batchSize, deltaWidth};
     const unsigned grid = (unsigned)((rows + 255) / 256);
-    ropekv::delta_metadata_kernel<<<grid, 256, 0, (cudaStream_t)stream>>>(a);
-    return launch_status();
+    return launch_k(ropekv::delta_metadata_kernel, grid, 256, (cudaStream_t)stream, false, a);
 }
 
 int dflash_gather_delta_rope(const float* source, float* output, const int32_t* deltaPositions,
@@ -649,8 +664,7 @@ int dflash_gather_delta_rope(const float* source, float* output, const int32_t* 
                             numDeltaTokens, batchSize, sourceRows, cacheCapacity, rotaryDim};
     const long long n = (long long)numDeltaTokens * (rotaryDim / 4);
     const unsigned grid = (unsigned)((n + 255) / 256);
-    ropekv::gather_delta_rope_kernel<<<grid, 256, 0, (cudaStream_t)stream>>>(a);
-    return launch_status();
+    return launch_k(ropekv::gather_delta_rope_kernel, grid, 256, (cudaStream_t)stream, false, a);
 }
 
 int rope_write_kv_slot_mapping(const float* cosSin, const int64_t* positions, const uint16_t* q,
@@ -670,7 +684,7 @@ int rope_write_kv_slot_mapping(const float* cosSin, const int64_t* positions, co
     if (numQHeads <= 0 || numKVHeads <= 0 || numQHeads % numKVHeads != 0)
         return ROPEKV_ERR_HEADS;
     if (numTokens < 0 || cosSinRows < 0 || numBlocks < 0 || blockSize <= 0 ||
-        numBlocks > (1LL << 40))
+        numBlocks > (1LL << 40) || numBlocks > INT64_MAX / blockSize)
         return ROPEKV_ERR_SHAPE;
     if (qTokenStride < (int64_t)numQHeads * headDim || kTokenStride < (int64_t)numKVHeads * headDim ||
         vTokenStride < (int64_t)numKVHeads * headDim || (qTokenStride % 8) != 0 ||
@@ -715,31 +729,16 @@ int rope_write_kv_slot_mapping(const float* cosSin, const int64_t* positions, co
     const unsigned grid = (unsigned)((long long)numTokens * sh.ctasPerUnit);
     cudaStream_t st = (cudaStream_t)stream;
     const bool gptj = style == ROPEKV_GPTJ;
-#define ROPEKV_SLOTMAP_LAUNCH(DD)                                                            \
-    do {                                                                                   \
-        if (!sh.small && !pdl_allowed(grid, sh))                                           \
-            gptj ? launch_k(ropekv::rope_kv_slotmap_kernel<DD, ropekv::kGptj, 2, kPolLarge>, \
-                            grid, sh.threads, st, false, a)                                \
-                 : launch_k(ropekv::rope_kv_slotmap_kernel<DD, ropekv::kNeox, 2, kPolLarge>, \
-                            grid, sh.threads, st, false, a);                               \
-        else if (!sh.small)                                                                \
-            gptj ? launch_k(ropekv::rope_kv_slotmap_kernel<DD, ropekv::kGptj, 2, kPolPdl>, \
-                            grid, sh.threads, st, true, a)                                 \
-                 : launch_k(ropekv::rope_kv_slotmap_kernel<DD, ropekv::kNeox, 2, kPolPdl>, \
-                            grid, sh.threads, st, true, a);                                \
-        else                                                                               \
-            gptj ? launch_small<ropekv::rope_kv_slotmap_kernel<DD, ropekv::kGptj, 2, kPolSmall>>( \
-                       grid, sh.threads, st, a)                                            \
-                 : launch_small<ropekv::rope_kv_slotmap_kernel<DD, ropekv::kNeox, 2, kPolSmall>>( \
-                       grid, sh.threads, st, a);                                           \
-    } while (0)
     switch (headDim) {
-    case 64: ROPEKV_SLOTMAP_LAUNCH(64); break;
-    case 128: ROPEKV_SLOTMAP_LAUNCH(128); break;
-    default: ROPEKV_SLOTMAP_LAUNCH(256); break;
+    case 64: return launch_slotmap<64>(a, gptj, grid, sh, st);
+    case 128: return launch_slotmap<128>(a, gptj, grid, sh, st);
+    default: return launch_slotmap<256>(a, gptj, grid, sh, st);
     }
-#undef ROPEKV_SLOTMAP_LAUNCH
-    return launch_status();
+}
+
+int ropekv_set_residency_cap(int enable)
+{
+    return g_residency_cap.exchange(enable ? 1 : 0, std::memory_order_relaxed);
 }
 
 int rope_check_capacity(int32_t cosSinSeqLen, int32_t kvCapacity)

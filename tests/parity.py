@@ -13,6 +13,8 @@ Comparison rule (element by element):
 """
 from __future__ import annotations
 
+import contextlib
+
 import numpy as np
 
 try:
@@ -27,8 +29,22 @@ TOL_ABS = 1e-6
 ULP_RULE_MIN = 2.0 ** -6
 
 
+_DEVICE = [None]
+
+
 def dev():
-    return torch.device("cuda:0")
+    """The device the helpers move inputs to (cuda:0 unless on_device says)."""
+    return _DEVICE[0] or torch.device("cuda:0")
+
+
+@contextlib.contextmanager
+def on_device(device):
+    """Run the helpers against `device` instead of cuda:0."""
+    _DEVICE[0] = device
+    try:
+        yield
+    finally:
+        _DEVICE[0] = None
 
 
 def to_dev(a: np.ndarray):
@@ -141,7 +157,7 @@ def run_gpu_contiguous(case: workloads.ContiguousCase, stream=None):
         else:
             rk.rope_write_kv_tree(cs, end, to_dev(case.pos_ids), qkv, cache, qout, case.Hq,
                                   case.Hkv, case.style, stream=stream)
-    torch.cuda.synchronize()
+    torch.cuda.synchronize(dev())
     return to_host_bits(qkv), to_host_bits(cache), (to_host_bits(qout) if qout is not None else None)
 
 

@@ -42,7 +42,7 @@ def test_header_declares_the_entry_points():
                      "dflash_prepare_delta_metadata", "dflash_gather_delta_rope",
                      "rope_write_kv_slot_mapping", "rope_write_kv_continuous_qknorm",
                      "rope_write_kv_continuous_fp8",
-                     "rope_check_capacity",
+                     "rope_check_capacity", "ropekv_set_residency_cap",
                      "ropekv_status_string"}
 
 
@@ -215,3 +215,47 @@ def test_fp8_rejects_bad_arguments(lib):
     assert f(A, A, A, MIS, A, A, A, ctypes.byref(d), NUL) == ERR["MISALIGNED"]
     assert f(A, A, A, A, A, A, A, ctypes.byref(_dims(rotaryDim=40)), NUL) == ERR["ROTARY_DIM"]
     assert f(NUL, NUL, NUL, NUL, NUL, NUL, NUL, ctypes.byref(_dims(seqLen=0)), NUL) == OK
+
+
+def test_slot_mapping_rejects_slot_counts_past_int64(lib):
+    # numBlocks * blockSize must not overflow: 2^40 blocks of 2^31 - 1 slots
+    assert _slotmap(lib, blocks=1 << 40, bsz=(1 << 31) - 1) == ERR["SHAPE"]
+
+
+def test_residency_cap_switch(lib):
+    # host-only: the switch is a process-wide flag; returns the previous value
+    try:
+        assert lib.ropekv_set_residency_cap(0) == 1          # on by default
+        assert lib.ropekv_set_residency_cap(0) == 0
+        assert rk.ropekv_set_residency_cap(True) is False
+        assert rk.ropekv_set_residency_cap(True) is True
+    finally:
+        lib.ropekv_set_residency_cap(1)
+
+
+def _no_cuda_device():
+    try:
+        import torch
+        return torch.cuda.device_count() == 0
+    except Exception:
+        return True
+
+
+@pytest.mark.skipif(not _no_cuda_device(),
+                    reason="fake device addresses must never reach a real GPU")
+def test_launch_failure_is_the_launchs_own_status(lib):
+    """On a host without a CUDA device every call that passes the host checks
+    reaches its launch, and the failure comes back from that launch as
+    ROPEKV_ERR_LAUNCH (no launch path reads CUDA's last-error state). The
+    fused update accepts a NULL cos/sin source when it has no source rows,
+    as the gather does."""
+    d = _dims()
+    assert lib.rope_write_kv_continuous(A, A, A, A, A, ctypes.byref(d), NUL) == ERR["LAUNCH"]
+    assert lib.rope_write_kv_packed(A, A, A, ctypes.byref(_dims(batch=1, seqLen=1)),
+                                    NUL) == ERR["LAUNCH"]
+    assert _paged(lib) == ERR["LAUNCH"]
+    assert lib.dflash_prepare_delta_metadata(A, A, 4, A, A, 4, NUL) == ERR["LAUNCH"]
+    assert lib.dflash_gather_delta_rope(NUL, A, A, A, NUL, 8, 4, 0, 64, 64, NUL) == ERR["LAUNCH"]
+    assert _slotmap(lib) == ERR["LAUNCH"]
+    assert _fused(lib, ptrs=[A, A, A, NUL, A, A, A, A, A], rows=0) == ERR["LAUNCH"]
+    assert _fused(lib, ptrs=[A, A, A, NUL, A, A, A, A, A], rows=1) == ERR["NULL"]

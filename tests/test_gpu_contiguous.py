@@ -221,17 +221,36 @@ def test_dependent_back_to_back_calls(B, S):
 
 @pytest.mark.parametrize("tokens", [1, 152, 153, 450, 608, 609, 1000, 1023])
 @pytest.mark.parametrize("norm", [False, True])
-def test_small_launch_residency_caps(tokens, norm):
+@pytest.mark.parametrize("cap_on", [True, False])
+def test_small_launch_residency_caps(tokens, norm, cap_on):
     """Decode-sized launches (fewer than 1024 tokens) reserve dynamic shared
     memory so that at most ceil(CTAs / SMs) CTAs share an SM: 1, 2, 3, 4, 5
     and 7 CTAs per SM here (the normalized call, two CTAs per token, also
-    crosses the 8-per-SM limit above which no memory is reserved). Every cap
-    gives the oracle's result."""
+    crosses the 8-per-SM limit above which no memory is reserved). Every cap,
+    and the cap switched off by the caller, gives the oracle's result."""
+    import rope_kv_cache_gb300 as rk
     case = workloads.make_continuous(tokens, 1, 8, 2, 128, 128, 16, NEOX, 5e5, seed=4000 + tokens,
                                      name=f"caps{tokens}")
     if norm:
         case.norm = workloads.norm_weights(4000 + tokens, 128)
-    check_contiguous(case)
+    prev = rk.ropekv_set_residency_cap(cap_on)
+    try:
+        check_contiguous(case)
+    finally:
+        rk.ropekv_set_residency_cap(prev)
+
+
+def test_tensors_on_a_non_current_device():
+    """The binding makes the tensors' device current for the call: a call
+    whose tensors live on cuda:1 while cuda:0 is current gives the oracle's
+    result (and sets up the residency cap on cuda:1)."""
+    if torch.cuda.device_count() < 2:
+        pytest.skip("needs two CUDA devices")
+    case = workloads.make_continuous(64, 1, 8, 2, 128, 128, 16, NEOX, 5e5, seed=77,
+                                     name="device1")
+    from parity import on_device
+    with on_device(torch.device("cuda:1")), torch.cuda.device(0):
+        check_contiguous(case)
 
 
 @pytest.mark.parametrize("B,S", [(4, 1), (2, 600)])

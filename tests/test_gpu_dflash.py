@@ -115,6 +115,25 @@ def test_fused_matches_oracle_and_pipeline(idx):
     assert np.array_equal(g, to_host_bits(_run_unfused(fc)))
 
 
+@pytest.mark.parametrize("style", [NEOX, GPTJ])
+def test_fused_without_source_rows(style):
+    """No cos/sin source rows (the source may then be NULL, as for the
+    gather): every row's cos/sin is zero, so rotated K dims are written as
+    zeros, exactly as the three-launch pipeline writes them."""
+    import oracle
+    fc = workloads.make_paged_fused(6, 21, 2, 128, 64, 8, 6, 40, style, 1e4, seed=350 + style,
+                                    len_range=(0, 21), unmapped_frac=0.05, name="fused_nosrc")
+    fc.source = np.ascontiguousarray(fc.source[:0])
+    g = to_host_bits(_run_fused(fc))
+    want = fc.new_pool()
+    oracle.paged_fused(fc.k_delta, fc.v_delta, want, fc.source, fc.old_lengths, fc.delta_lengths,
+                       fc.W, None, fc.page_table, fc.style)
+    compare(g, want, pool_rotated(want.shape, fc.r), fc.name)
+    assert np.array_equal(g, to_host_bits(_run_unfused(fc)))
+    written = want[0] != workloads.SENTINEL
+    assert written.any() and np.all(want[0][..., : fc.r][written[..., : fc.r]] == 0)
+
+
 def test_config_paged_fused_full():
     """16384 rows into the 17.2 GB pool: every written row against the oracle
     composition, nothing else changed, and bit-identical to the pipeline."""
