@@ -40,7 +40,7 @@ import workloads  # noqa: E402
 
 METRIC = "fused RoPE+KV-write tokens/s and effective HBM GB/s (% of GB300 peak)"
 HEADLINE = "prefill"
-EXTRA = ("decode", "tree", "paged", "packed_tiny", "paged_fused", "paged_fused_3launch",
+EXTRA = ("decode", "decode_floor", "tree", "paged", "packed_tiny", "paged_fused", "paged_fused_3launch",
          "slotmap_prefill", "slotmap_decode", "prefill_qknorm", "decode_qknorm", "prefill_fp8",
          "decode_fp8")
 NOMINAL_HBM_GBS = 8000.0
@@ -68,6 +68,10 @@ DESCR = {
     "decode_qknorm": "the decode with pre-RoPE QK RMS norm fused in (weights [128], eps 1e-6)",
     "prefill_fp8": "the prefill with an E4M3 KV cache (k_scale 0.05, v_scale 0.04)",
     "decode_fp8": "the decode with an E4M3 KV cache (k_scale 0.05, v_scale 0.04)",
+    "decode_floor": "the floor of one dependent decode-sized launch: a plain copy of decode's "
+                    "bytes in decode's grid (256 CTAs x 192 threads, four 16-byte vectors per "
+                    "thread), with decode's L2 prefetch, dependent-launch attribute and residency "
+                    "cap, timed like decode",
     "decode_c1024": "decode as above with cache capacity 1024 (profiler-sized twin)",
     "paged_p8192": "paged as above with 64 pages/seq and 8192 pages per plane (profiler-sized twin)",
     "paged_fused_p8192": "paged_fused with 64 pages/seq and 8192 pages per plane (profiler-sized twin)",
@@ -342,6 +346,39 @@ class DeviceWorkload:
                                         c.Hq, c.Hkv, c.style, stream=stream)
 
 
+class FloorWorkload:
+    """The decode floor (include/ropekv_floor.h): per step one copy of the
+    decode call's bytes in the decode call's grid -- 256 CTAs of 192 threads,
+    four 16-byte vectors per thread, read and written -- through a ring of
+    source/destination buffers larger than twice the L2."""
+    THREADS = 192
+    CTAS = 256
+
+    def __init__(self, name: str, device, l2_bytes: int):
+        import torch
+        import rope_kv_cache_gb300 as rk
+        self.torch, self.rk, self.name, self.device = torch, rk, name, device
+        self.three_launch = self.paged = self.fused = self.slotmap = False
+        self.copy_bytes = self.CTAS * self.THREADS * 4 * 16
+        self.bytes = 2 * self.copy_bytes
+        self.tokens = self.CTAS
+        self.ring = max(2, min(96, math.ceil(2 * l2_bytes / self.bytes)))
+        n = self.copy_bytes // 2
+        self.sets = [(torch.randint(-2 ** 15, 2 ** 15, (n,), dtype=torch.int16, device=device),
+                      torch.empty(n, dtype=torch.int16, device=device)) for _ in range(self.ring)]
+        torch.cuda.synchronize(device)
+
+    def call(self, k: int, stream):
+        src, dst = self.sets[k % self.ring]
+        self.rk.ropekv_floor_copy(src, dst, self.THREADS, True, stream=stream)
+
+
+def make_workload(name: str, device, l2_bytes: int):
+    if name == "decode_floor":
+        return FloorWorkload(name, device, l2_bytes)
+    return DeviceWorkload(name, device, l2_bytes)
+
+
 def make_graphs(wl: DeviceWorkload, steps: int, stream, chunk: int = 256):
     """CUDA graphs holding exactly `steps` launches: full chunks plus a tail."""
     torch = wl.torch
@@ -485,139 +522,261 @@ def e2e_contiguous(wl: DeviceWorkload, steps: int):
 
 
 # ------------------------------------------------------------ CPU oracle --
+#
+# The CPU baseline is the oracle as it stands, timed on the host cores. A
+# workload is cut into small independent oracle calls ("units") whose outputs
+# land in small host buffers, so that no 8.6 GB cache or 17 GB pool is
+# allocated on the host; the arithmetic per token is the oracle's, unchanged:
+#   * contiguous-cache calls: one chunk of one sequence as a B = 1 call, with
+#     the chunk's own slots and positions (the end length shifted to match);
+#   * paged update: a chunk of delta rows through oracle.paged_rows (the
+#     destinations and values; the pool write is a copy of those values);
+#   * fused DFlash step: one sequence through oracle.delta_metadata,
+#     oracle.gather_delta_rope and oracle.paged_rows (the oracle's own
+#     composition of the three steps, without the pool);
+#   * slot mapping: a chunk of tokens, their slots renumbered into a
+#     chunk-sized cache.
+# The oracle is single-threaded; all cores are used by running independent
+# units in one spawned process per core.
 
-_HEADLINE_CASE = []
-
-
-def headline_case():
-    """The headline workload's inputs, drawn once per process."""
-    if not _HEADLINE_CASE:
-        _HEADLINE_CASE.append(workloads.config(HEADLINE))
-    return _HEADLINE_CASE[0]
-
-
-def oracle_sample(budget_s: float, max_tokens_per_call: int = 2048):
-    """Time the oracle (single thread) on prefill-shaped sub-problems: the
-    first `n` tokens of one sequence at a time, for about budget_s seconds.
-    The output buffers are allocated once and rewritten by every call."""
-    import oracle
-    c = headline_case()
-    n = min(max_tokens_per_call, c.S)
-    done = 0
-    calls = 0
-    cache = workloads.sentinel_fill((1, 2, c.Hkv, c.cap, c.D))
-    qout = workloads.sentinel_fill((1, n, c.Hq, c.D))
-    t0 = time.perf_counter()
-    while True:
-        b = calls % c.B
-        qkv = np.ascontiguousarray(c.qkv[b:b + 1, :n])
-        end = np.array([c.end_lens[b] - c.S + n], dtype=np.int32)
-        oracle.continuous(c.cos_sin, end, qkv, cache, qout, c.Hq, c.Hkv, c.style)
-        done += n
-        calls += 1
-        if time.perf_counter() - t0 >= budget_s:
-            break
-    sec = time.perf_counter() - t0
-    return done, sec, calls, n
+def _oracle_base_name(name: str) -> str:
+    return name[: -len("_3launch")] if name.endswith("_3launch") else name
 
 
-# Parallel oracle: the unchanged oracle run in one spawned process per host
-# core, each on its own prefill sequence slice (the oracle is single-threaded;
-# running independent sub-problems side by side is how it uses all cores).
+class OracleUnits:
+    """A workload's inputs cut into oracle calls of about `chunk` tokens."""
+
+    def __init__(self, name: str, chunk: int = 128):
+        self.name = name
+        c = workloads.config(_oracle_base_name(name))
+        self.case = c
+        self.calls = []          # (callable, tokens it processes)
+        if isinstance(c, workloads.PagedCase):
+            kw, vw = c.plane_written()
+            valid = kw | vw
+            for t0 in range(0, c.N, chunk):
+                sl = slice(t0, min(c.N, t0 + chunk))
+                args = (np.ascontiguousarray(c.k_delta[sl]), np.ascontiguousarray(c.v_delta[sl]),
+                        np.ascontiguousarray(c.cos_sin_rows[sl]),
+                        np.ascontiguousarray(c.positions[sl]),
+                        np.ascontiguousarray(c.seq_ids[sl]))
+                self.calls.append((self._paged_call(args), int(valid[sl].sum())))
+            self.units_total = c.valid_rows
+        elif isinstance(c, workloads.PagedFusedCase):
+            kw, vw = c.plane_written()
+            valid = (kw | vw).reshape(c.B, c.W)
+            for b in range(c.B):
+                self.calls.append((self._fused_call(b), int(valid[b].sum())))
+            self.units_total = c.valid_rows
+        elif isinstance(c, workloads.SlotMapCase):
+            for t0 in range(0, c.T, chunk):
+                n = min(c.T, t0 + chunk) - t0
+                self.calls.append((self._slotmap_call(t0, n), n))
+            self.units_total = c.T
+        else:
+            self._cache = (np.zeros((1, 2, c.Hkv, c.cap, c.D), dtype=np.uint8)
+                           if c.fp8_scales is not None else
+                           np.zeros((1, 2, c.Hkv, c.cap, c.D), dtype=np.uint16))
+            if c.mode == "packed":
+                self.calls.append((self._packed_call(), c.tokens))
+            else:
+                n = min(chunk, c.S)
+                self._qout = np.zeros((1, n, c.Hq, c.D), dtype=np.uint16)
+                for b in range(c.B):
+                    for s0 in range(0, c.S, n):
+                        m = min(c.S, s0 + n) - s0
+                        self.calls.append((self._contiguous_call(b, s0, m), m))
+            self.units_total = c.tokens
+        self.bytes_per_unit = c.algorithmic_bytes() / max(1, self.units_total)
+
+    def _contiguous_call(self, b, s0, m):
+        import oracle
+        c = self.case
+        qkv = np.ascontiguousarray(c.qkv[b:b + 1, s0:s0 + m])
+        end = np.array([int(c.end_lens[b]) - c.S + s0 + m], dtype=np.int32)
+        pos = np.ascontiguousarray(c.pos_ids[b:b + 1, s0:s0 + m]) if c.mode == "tree" else None
+        qout = self._qout[:, :m] if m == self._qout.shape[1] else np.zeros(
+            (1, m, c.Hq, c.D), dtype=np.uint16)
+        cache = self._cache
+
+        def run():
+            if c.mode == "tree":
+                oracle.tree(c.cos_sin, end, pos, qkv, cache, qout, c.Hq, c.Hkv, c.style)
+            elif c.norm is not None:
+                qw, kw, eps = c.norm
+                oracle.continuous_qknorm(c.cos_sin, end, qkv, cache, qout, qw, kw, eps, c.Hq,
+                                         c.Hkv, c.style)
+            elif c.fp8_scales is not None:
+                oracle.continuous_fp8(c.cos_sin, end, qkv, cache, qout, c.fp8_scales[0],
+                                      c.fp8_scales[1], c.Hq, c.Hkv, c.style)
+            else:
+                oracle.continuous(c.cos_sin, end, qkv, cache, qout, c.Hq, c.Hkv, c.style)
+        return run
+
+    def _packed_call(self):
+        import oracle
+        c = self.case
+        qkv = c.qkv.copy()
+
+        def run():
+            oracle.packed(c.cos_sin, qkv, self._cache, c.Hq, c.Hkv, c.style)
+        return run
+
+    def _paged_call(self, args):
+        import oracle
+        c = self.case
+        k, v, cs, pos, seq = args
+
+        def run():
+            oracle.paged_rows(k, v, cs, pos, seq, c.page_table, c.num_pages, c.tokens_per_page,
+                              c.style)
+        return run
+
+    def _fused_call(self, b):
+        import oracle
+        c = self.case
+        W = c.W
+        old = np.ascontiguousarray(c.old_lengths[b:b + 1])
+        lens = np.ascontiguousarray(c.delta_lengths[b:b + 1])
+        state = np.ascontiguousarray(c.state[b:b + 1]) if c.state is not None else None
+        table = np.ascontiguousarray(c.page_table[b:b + 1])
+        k = np.ascontiguousarray(c.k_delta[b * W:(b + 1) * W])
+        v = np.ascontiguousarray(c.v_delta[b * W:(b + 1) * W])
+
+        def run():
+            pos, seq = oracle.delta_metadata(old, lens, W)
+            cs = oracle.gather_delta_rope(c.source, pos, seq, state, 1)
+            oracle.paged_rows(k, v, cs, pos, seq, table, c.num_pages, c.tokens_per_page, c.style)
+        return run
+
+    def _slotmap_call(self, t0, n):
+        import oracle
+        c = self.case
+        qkv = np.ascontiguousarray(c.qkv[t0:t0 + n])
+        pos = np.ascontiguousarray(c.positions[t0:t0 + n])
+        slots = np.where(c.slots[t0:t0 + n] >= 0, np.arange(n), -1).astype(np.int64)
+        blocks = -(-n // c.block_size)
+        kc = np.zeros((blocks, c.block_size, c.Hkv, c.D), dtype=np.uint16)
+        vc = np.zeros_like(kc)
+        qout = np.zeros((n, c.Hq, c.D), dtype=np.uint16)
+        Hq, Hkv = c.Hq, c.Hkv
+
+        def run():
+            oracle.slot_mapping(c.cos_sin, pos, qkv[:, :Hq], qkv[:, Hq:Hq + Hkv],
+                                qkv[:, Hq + Hkv:], slots, kc, vc, qout, None, c.style)
+        return run
+
+    def run_units(self, first: int, count: int = 0, budget_s: float = 0.0):
+        """Run units first, first+1, ... (wrapping): `count` of them, or as many
+        as `budget_s` seconds allow (at least one). Returns (tokens, seconds)."""
+        done, k = 0, 0
+        n = len(self.calls)
+        t0 = time.perf_counter()
+        while True:
+            fn, toks = self.calls[(first + k) % n]
+            fn()
+            done += toks
+            k += 1
+            if (count and k >= count) or (not count and time.perf_counter() - t0 >= budget_s):
+                break
+        return done, time.perf_counter() - t0
+
+
 _W = {}
 
 
-def _oracle_worker_init(cos_sin, slices, end_by_b, Hq, Hkv, style, cap, D):
-    n = slices[0].shape[1]
-    _W.update(cos_sin=cos_sin, slices=slices, end=end_by_b, Hq=Hq, Hkv=Hkv, style=style,
-              cache=workloads.sentinel_fill((1, 2, Hkv, cap, D)),
-              qout=workloads.sentinel_fill((1, n, Hq, D)))
+def _oracle_worker(job):
+    """Pool worker: (name, chunk, first unit, count, budget) -> (tokens, seconds).
+    Keeps the last workload's units, so that consecutive jobs reuse them."""
+    name, chunk, first, count, budget_s = job
+    key = (name, chunk)
+    if _W.get("key") != key:
+        import oracle
+        oracle.build()
+        _W.clear()
+        _W["units"] = OracleUnits(name, chunk)
+        _W["key"] = key
+    return _W["units"].run_units(first, count, budget_s)
 
 
-def _oracle_worker_run(job):
-    """Run oracle.continuous on sequence slice b, `calls` times or for
-    `budget_s` seconds; returns (tokens, seconds) of this worker's own loop."""
-    b, calls, budget_s = job
-    import oracle
-    w = _W
-    qkv = w["slices"][b]
-    n = qkv.shape[1]
-    end = np.array([w["end"][b]], dtype=np.int32)
-    done, k = 0, 0
-    t0 = time.perf_counter()
-    while True:
-        oracle.continuous(w["cos_sin"], end, qkv, w["cache"], w["qout"], w["Hq"], w["Hkv"],
-                          w["style"])
-        done += n
-        k += 1
-        if (calls and k >= calls) or (not calls and time.perf_counter() - t0 >= budget_s):
-            break
-    return done, time.perf_counter() - t0
-
-
-def oracle_pool(n_tokens: int):
-    """A spawn-started pool of one oracle worker per host core, each holding
-    the first n_tokens tokens of every prefill sequence."""
+def oracle_process_pool():
+    """One spawn-started process per host core (spawn: nothing of the parent's
+    CUDA state is inherited)."""
     import multiprocessing
     import oracle
     oracle.build()
-    c = headline_case()
-    n = min(n_tokens, c.S)
-    slices = [np.ascontiguousarray(c.qkv[b:b + 1, :n]) for b in range(c.B)]
-    end_by_b = [int(c.end_lens[b] - c.S + n) for b in range(c.B)]
     procs = max(1, os.cpu_count() or 1)
-    ctx = multiprocessing.get_context("spawn")
-    pool = ctx.Pool(procs, initializer=_oracle_worker_init,
-                    initargs=(c.cos_sin, slices, end_by_b, c.Hq, c.Hkv, c.style, c.cap, c.D))
-    return pool, procs, n, c.B
+    return multiprocessing.get_context("spawn").Pool(procs), procs
 
 
-def oracle_sample_parallel(budget_s: float, n_tokens: int = 512):
-    """Aggregate oracle throughput with every host core busy: the sum of the
-    workers' own token rates over about budget_s seconds each."""
-    pool, procs, n, nb = oracle_pool(n_tokens)
-    try:
-        pool.map(_oracle_worker_run, [(k % nb, 1, 0.0) for k in range(procs)])  # warm-up
-        res = pool.map(_oracle_worker_run, [(k % nb, 0, budget_s) for k in range(procs)])
-    finally:
-        pool.close()
-        pool.join()
-    rate = sum(d / t for d, t in res)
-    return rate, procs, n, sum(d for d, _ in res)
+def oracle_rates(names, single_s: float, parallel_s: float, pool, procs) -> dict:
+    """For every workload: the oracle's single-thread rate (this process) and
+    its all-core rate (the sum of the pool processes' own rates)."""
+    out = {}
+    for name in names:
+        units = OracleUnits(name)
+        units.run_units(0, count=1)                       # warm-up
+        tok1, sec1 = units.run_units(1, budget_s=single_s)
+        n = len(units.calls)
+        stride = max(1, n // procs)
+        pool.map(_oracle_worker, [(name, 128, (j * stride) % n, 1, 0.0) for j in range(procs)])
+        res = pool.map(_oracle_worker, [(name, 128, (j * stride + 1) % n, 0, parallel_s)
+                                        for j in range(procs)])
+        rate = sum(d / t for d, t in res)
+        out[name] = {
+            "value": rate, "unit": "tokens/s", "cores": procs, "kind": "oracle",
+            "effective_gbs": rate * units.bytes_per_unit / 1e9,
+            "sample": f"{procs} spawned processes, each running oracle calls of <= 128 tokens "
+                      f"(rows) of this workload for {parallel_s:g} s "
+                      f"({sum(d for d, _ in res)} tokens in all); value = sum of the "
+                      f"processes' rates",
+            "single_thread": {"value": tok1 / sec1, "cores": 1,
+                              "effective_gbs": tok1 / sec1 * units.bytes_per_unit / 1e9,
+                              "sample": f"{tok1} tokens in {sec1:.2f} s"},
+        }
+        del units
+    return out
 
 
 def run_reference(args):
-    """The reference arm: the CPU oracle as it stands, one spawned process per
-    host core, each step one call per process on its own sequence slice."""
+    """The reference arm: the CPU oracle as it stands on the headline workload,
+    one spawned process per host core; every step, each process runs one
+    oracle call on its own chunk of a prefill sequence, the chunk sized so
+    that warm-up and timed steps take about a minute."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    # tokens per call sized so warm-up + timed steps take about a minute
     per_tok_s = 1.0 / 6000.0
-    want = int(max(1, 60.0 / per_tok_s / max(1, args.steps + args.warmup)))
-    pool, procs, n, nb = oracle_pool(want)
+    chunk = int(max(1, min(2048, 60.0 / per_tok_s / max(1, args.steps + args.warmup))))
+    pool, procs = oracle_process_pool()
     try:
+        n_units = len(OracleUnits(HEADLINE, chunk).calls)
+        done = []
+
         def step(k):
-            pool.map(_oracle_worker_run, [((k + j) % nb, 1, 0.0) for j in range(procs)])
+            res = pool.map(_oracle_worker, [(HEADLINE, chunk, (k * procs + j) % n_units, 1, 0.0)
+                                            for j in range(procs)])
+            done.append(sum(d for d, _ in res))
 
         for k in range(args.warmup):
             step(k)
+        done.clear()
         t0 = time.perf_counter()
         for k in range(args.steps):
-            step(k)
+            step(args.warmup + k)
         sec = time.perf_counter() - t0
     finally:
         pool.close()
         pool.join()
-    value = procs * n * args.steps / sec
+    value = sum(done) / sec
     sample = (f"oracle.continuous in {procs} spawned processes, one call per process per step on "
-              f"{n} tokens of one prefill sequence each")
+              f"{chunk} tokens of one prefill sequence each")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": sec * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1) FP16 QKV)",
-        "config": {"workload": DESCR[HEADLINE], "tokens_per_step": procs * n},
+        "config": {"workload": DESCR[HEADLINE], "tokens_per_step": sum(done) // args.steps},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": procs, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -637,13 +796,16 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=HEADLINE,
                     choices=list(workloads.CONFIG_NAMES) + list(workloads.PROFILE_NAMES)
-                    + list(workloads.NEXT_NAMES),
+                    + list(workloads.NEXT_NAMES) + ["decode_floor"],
                     help="workload of the headline line (default: the prefill)")
     ap.add_argument("--extra-steps", type=int, default=4000,
                     help="timed launches per extra workload (decode, tree, paged, packed_tiny)")
     ap.add_argument("--no-extra", action="store_true", help="headline workload only")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
-                    help="CPU time budget of the oracle baseline sample")
+                    help="CPU time budget of the headline's oracle baseline sample "
+                         "(single thread, then all cores)")
+    ap.add_argument("--cpu-seconds-extra", type=float, default=1.5,
+                    help="the same for every other workload")
     ap.add_argument("--e2e-steps", type=int, default=100)
     args = ap.parse_args(argv)
     if args.warmup < 3:
@@ -677,7 +839,7 @@ def main(argv=None):
     stream = torch.cuda.Stream(dev)
 
     name = args.workload
-    wl = DeviceWorkload(name, dev, l2)
+    wl = make_workload(name, dev, l2)
     sec, t0, t1 = time_steps(wl, args.steps, args.warmup, stream, barrier)
     if world > 1:
         sec = max_over_ranks(sec, dist, dev)
@@ -685,8 +847,9 @@ def main(argv=None):
     achieved = wl.bytes / launch_s / 1e9
     clocks = sampler.summary(t0, t1) if sampler else None
     e2e = e2e_contiguous(wl, args.e2e_steps) \
-        if not (wl.paged or wl.fused or wl.slotmap or wl.case.norm is not None
-                or wl.case.fp8_scales is not None) else None
+        if isinstance(wl, DeviceWorkload) and not (
+            wl.paged or wl.fused or wl.slotmap or wl.case.norm is not None
+            or wl.case.fp8_scales is not None) else None
     tokens, bytes_step, ring = wl.tokens, wl.bytes, wl.ring
     kernel = _kernel_name(wl)
     del wl
@@ -697,7 +860,7 @@ def main(argv=None):
         for xname in EXTRA:
             if xname == name:
                 continue
-            w = DeviceWorkload(xname, dev, l2)
+            w = make_workload(xname, dev, l2)
             s_, _, _ = time_steps(w, args.extra_steps, args.warmup, stream, barrier)
             per = s_ / args.extra_steps
             gbs = w.bytes / per / 1e9
@@ -711,6 +874,17 @@ def main(argv=None):
                             "dram_bytes_per_launch_ncu": ncu_traffic(xname)}
             del w
             torch.cuda.empty_cache()
+        floor = extra.get("decode_floor")
+        if floor is not None:
+            # decode-sized launches as a fraction of the floor of one dependent
+            # launch in the same grid (time ratio: 1.0 = at the floor)
+            floor["cpu_baseline"] = None
+            floor["note"] = "a measurement reference, not a workload of the method: no oracle"
+            for xname in ("decode", "decode_qknorm", "decode_fp8", "slotmap_decode"):
+                if xname in extra:
+                    extra[xname]["floor_us_per_launch"] = floor["us_per_launch"]
+                    extra[xname]["frac_of_floor"] = (floor["us_per_launch"]
+                                                     / extra[xname]["us_per_launch"])
     if sampler:
         sampler.stop()
     if world > 1:
@@ -718,8 +892,24 @@ def main(argv=None):
     if rank != 0:
         return 0
 
-    cpu_tokens, cpu_sec, cpu_calls, cpu_n = oracle_sample(args.cpu_seconds)
-    par_rate, par_procs, par_n, par_tokens = oracle_sample_parallel(args.cpu_seconds)
+    pool, procs = oracle_process_pool()
+    try:
+        cpu = {name: None}
+        if name != "decode_floor":
+            cpu = oracle_rates([name], args.cpu_seconds, args.cpu_seconds, pool, procs)
+        if extra:
+            cpu.update(oracle_rates([x for x in EXTRA if x in extra and x != "decode_floor"
+                                     and not x.endswith("_3launch")],
+                                    args.cpu_seconds_extra, args.cpu_seconds_extra, pool, procs))
+    finally:
+        pool.close()
+        pool.join()
+    for xname, entry in extra.items():
+        base = cpu.get(_oracle_base_name(xname))
+        if base is not None:
+            entry["cpu_baseline"] = dict(base)
+            if xname.endswith("_3launch"):
+                entry["cpu_baseline"]["note"] = "the same oracle work as the one-launch step"
     line = {
         "metric": METRIC,
         "value": whole_job_rate(world, tokens, args.steps, sec),
@@ -747,16 +937,7 @@ def main(argv=None):
                      "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs, burst copy)"
                      if peak_src == "measured" else "fallback 6.8 TB/s",
                      "kernel": kernel},
-        "cpu_baseline": {"value": par_rate, "unit": "tokens/s", "cores": par_procs,
-                         "kind": "oracle",
-                         "sample": f"{par_procs} spawned processes, each calling oracle.continuous "
-                                   f"on {par_n} tokens of one prefill sequence for "
-                                   f"{args.cpu_seconds:.0f} s ({par_tokens} tokens in all); "
-                                   f"value = sum of the processes' rates",
-                         "single_thread": {
-                             "value": cpu_tokens / cpu_sec, "cores": 1,
-                             "sample": f"{cpu_calls} calls on {cpu_n} tokens of one prefill "
-                                       f"sequence ({cpu_tokens} tokens, {cpu_sec:.1f} s)"}},
+        "cpu_baseline": cpu[name],
         "e2e": e2e,
         "gpu_launches": args.steps,
         "clocks": clocks,
@@ -767,6 +948,8 @@ def main(argv=None):
 
 
 def _kernel_name(wl) -> str:
+    if isinstance(wl, FloorWorkload):
+        return "floor_copy_kernel (libropekv_floor.so)"
     c = wl.case
     if wl.slotmap:
         return f"rope_kv_slotmap_kernel<D={c.D}, {'NeoX' if c.style == 0 else 'GPT-J'}>"

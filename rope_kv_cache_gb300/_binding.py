@@ -22,7 +22,10 @@ GPTJ = 1
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "lib", "libropekv.so")
 
+FLOOR_LIB_PATH = os.path.join(_PKG, "lib", "libropekv_floor.so")
+
 _lib = None
+_floor_lib = None
 
 
 class RopeKVError(RuntimeError):
@@ -106,6 +109,40 @@ def ropekv_set_residency_cap(enable: bool) -> bool:
     process-wide; returns the previous setting. Results are identical either
     way; see include/ropekv.h for what the cap costs concurrent kernels."""
     return bool(load_library().ropekv_set_residency_cap(1 if enable else 0))
+
+
+def load_floor_library():
+    """Load libropekv_floor.so (the benchmark's decode-floor copy) once."""
+    global _floor_lib
+    if _floor_lib is None:
+        if not os.path.exists(FLOOR_LIB_PATH):
+            raise RuntimeError(f"{FLOOR_LIB_PATH} is not built")
+        lib = ctypes.CDLL(FLOOR_LIB_PATH)
+        lib.ropekv_floor_copy.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                                          ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p]
+        lib.ropekv_floor_copy.restype = ctypes.c_int
+        _floor_lib = lib
+    return _floor_lib
+
+
+def ropekv_floor_copy(src: torch.Tensor, dst: torch.Tensor, threads_per_cta: int = 192,
+                      cap: bool = True, stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Copy src to dst (same size, contiguous, on one device) with the launch
+    shape and policy of the library's decode-sized launches
+    (include/ropekv_floor.h). A measurement reference, not part of the path."""
+    if src.numel() * src.element_size() != dst.numel() * dst.element_size():
+        raise ValueError("src and dst must have the same size in bytes")
+    dev = src.device
+    for name, t in (("src", src), ("dst", dst)):
+        if t.device != dev or not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous on {dev}")
+    with torch.cuda.device(dev):
+        rc = load_floor_library().ropekv_floor_copy(
+            ctypes.c_void_p(src.data_ptr()), ctypes.c_void_p(dst.data_ptr()),
+            src.numel() * src.element_size(), int(threads_per_cta), 1 if cap else 0,
+            _stream_handle(stream, dev))
+    if rc != 0:
+        raise RuntimeError(f"ropekv_floor_copy: status {rc}")
 
 
 def ropekv_status_string(status: int) -> str:

@@ -259,3 +259,22 @@ def test_launch_failure_is_the_launchs_own_status(lib):
     assert _slotmap(lib) == ERR["LAUNCH"]
     assert _fused(lib, ptrs=[A, A, A, NUL, A, A, A, A, A], rows=0) == ERR["LAUNCH"]
     assert _fused(lib, ptrs=[A, A, A, NUL, A, A, A, A, A], rows=1) == ERR["NULL"]
+
+
+def test_floor_library_exports_and_checks():
+    """libropekv_floor.so (the benchmark's decode-floor copy) exports what
+    include/ropekv_floor.h declares and rejects bad arguments on the host."""
+    text = open(os.path.join(ROOT, "include", "ropekv_floor.h")).read()
+    names = re.findall(r"ROPEKV_FLOOR_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
+    assert names == ["ropekv_floor_copy"]
+    build.build_library()
+    fl = rk._binding.load_floor_library()
+    for n in names:
+        assert hasattr(fl, n)
+    f = fl.ropekv_floor_copy
+    per = 16 * 4 * 192
+    assert f(NUL, A, per, 192, 1, NUL) == -1
+    assert f(MIS, A, per, 192, 1, NUL) == -2
+    assert f(A, A, per, 100, 1, NUL) == -6          # not a multiple of 32
+    assert f(A, A, per + 16, 192, 1, NUL) == -6     # not whole CTAs
+    assert f(A, A, 0, 192, 1, NUL) == -6

@@ -131,7 +131,8 @@ def test_fused_without_source_rows(style):
     compare(g, want, pool_rotated(want.shape, fc.r), fc.name)
     assert np.array_equal(g, to_host_bits(_run_unfused(fc)))
     written = want[0] != workloads.SENTINEL
-    assert written.any() and np.all(want[0][..., : fc.r][written[..., : fc.r]] == 0)
+    rot = want[0][..., : fc.r][written[..., : fc.r]].view(np.float16)
+    assert written.any() and np.all(rot == 0)            # +0 or -0
 
 
 def test_config_paged_fused_full():
