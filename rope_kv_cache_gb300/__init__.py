@@ -16,6 +16,7 @@ from ._binding import (  # noqa: F401
     paged_kv_delta_update,
     paged_kv_delta_update_fused,
     rope_check_capacity,
+    ropekv_floor_copy,
     ropekv_set_residency_cap,
     rope_write_kv_continuous,
     rope_write_kv_continuous_fp8,
@@ -33,5 +34,5 @@ __all__ = [
     "rope_write_kv_tree",
     "paged_kv_delta_update", "paged_kv_delta_update_fused", "dflash_prepare_delta_metadata",
     "dflash_gather_delta_rope", "rope_write_kv_slot_mapping", "rope_check_capacity",
-    "ropekv_set_residency_cap", "ropekv_status_string",
+    "ropekv_set_residency_cap", "ropekv_floor_copy", "ropekv_status_string",
 ]
