@@ -69,13 +69,17 @@ DESCR = {
     "prefill_fp8": "the prefill with an E4M3 KV cache (k_scale 0.05, v_scale 0.04)",
     "decode_fp8": "the decode with an E4M3 KV cache (k_scale 0.05, v_scale 0.04)",
     "decode_floor": "the floor of one dependent decode-sized launch: a plain copy of decode's "
-                    "bytes in decode's grid (256 CTAs x 192 threads, four 16-byte vectors per "
+                    "bytes in decode's grid (512 CTAs x 96 threads, four 16-byte vectors per "
                     "thread), with decode's L2 prefetch, dependent-launch attribute and residency "
                     "cap, timed like decode",
     "decode_c1024": "decode as above with cache capacity 1024 (profiler-sized twin)",
     "paged_p8192": "paged as above with 64 pages/seq and 8192 pages per plane (profiler-sized twin)",
     "paged_fused_p8192": "paged_fused with 64 pages/seq and 8192 pages per plane (profiler-sized twin)",
     "slotmap_prefill_b4096": "slotmap_prefill with 4096 blocks per cache (profiler-sized twin)",
+    "slotmap_decode_b4096": "slotmap_decode with 4096 blocks per cache (profiler-sized twin)",
+    "decode_qknorm_c1024": "decode_qknorm with cache capacity 1024 (profiler-sized twin)",
+    "decode_fp8_c1024": "decode_fp8 with cache capacity 1024 (profiler-sized twin)",
+    "paged_fused_p8192_3launch": "paged_fused_p8192 as three launches (profiler-sized twin)",
 }
 
 
@@ -348,11 +352,11 @@ class DeviceWorkload:
 
 class FloorWorkload:
     """The decode floor (include/ropekv_floor.h): per step one copy of the
-    decode call's bytes in the decode call's grid -- 256 CTAs of 192 threads,
-    four 16-byte vectors per thread, read and written -- through a ring of
-    source/destination buffers larger than twice the L2."""
-    THREADS = 192
-    CTAS = 256
+    decode call's bytes in the decode call's grid -- two CTAs of 96 threads per
+    token, 512 in all, four 16-byte vectors per thread, read and written --
+    through a ring of source/destination buffers larger than twice the L2."""
+    THREADS = 96
+    CTAS = 512
 
     def __init__(self, name: str, device, l2_bytes: int):
         import torch
@@ -796,14 +800,16 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=HEADLINE,
                     choices=list(workloads.CONFIG_NAMES) + list(workloads.PROFILE_NAMES)
-                    + list(workloads.NEXT_NAMES) + ["decode_floor"],
+                    + list(workloads.NEXT_NAMES)
+                    + ["decode_floor", "paged_fused_3launch", "paged_fused_p8192_3launch"],
                     help="workload of the headline line (default: the prefill)")
     ap.add_argument("--extra-steps", type=int, default=4000,
                     help="timed launches per extra workload (decode, tree, paged, packed_tiny)")
     ap.add_argument("--no-extra", action="store_true", help="headline workload only")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU time budget of the headline's oracle baseline sample "
-                         "(single thread, then all cores)")
+                         "(single thread, then all cores); 0 leaves the CPU baseline out "
+                         "(profiling runs)")
     ap.add_argument("--cpu-seconds-extra", type=float, default=1.5,
                     help="the same for every other workload")
     ap.add_argument("--e2e-steps", type=int, default=100)
@@ -892,18 +898,20 @@ def main(argv=None):
     if rank != 0:
         return 0
 
-    pool, procs = oracle_process_pool()
-    try:
-        cpu = {name: None}
-        if name != "decode_floor":
-            cpu = oracle_rates([name], args.cpu_seconds, args.cpu_seconds, pool, procs)
-        if extra:
-            cpu.update(oracle_rates([x for x in EXTRA if x in extra and x != "decode_floor"
-                                     and not x.endswith("_3launch")],
-                                    args.cpu_seconds_extra, args.cpu_seconds_extra, pool, procs))
-    finally:
-        pool.close()
-        pool.join()
+    cpu = {name: None}
+    if args.cpu_seconds > 0:
+        pool, procs = oracle_process_pool()
+        try:
+            if name != "decode_floor":
+                cpu = oracle_rates([name], args.cpu_seconds, args.cpu_seconds, pool, procs)
+            if extra:
+                cpu.update(oracle_rates([x for x in EXTRA if x in extra and x != "decode_floor"
+                                         and not x.endswith("_3launch")],
+                                        args.cpu_seconds_extra, args.cpu_seconds_extra, pool,
+                                        procs))
+        finally:
+            pool.close()
+            pool.join()
     for xname, entry in extra.items():
         base = cpu.get(_oracle_base_name(xname))
         if base is not None:

@@ -41,9 +41,12 @@ int check_head_dims(int32_t D, int32_t r)
 //     30.30 us this way against 30.60 us with three 64-thread CTAs per token
 //     (no dependent launch: at that CTA count its launch-rate cap hurt), and
 //     the 4096-token tree 15.96 against 16.02 us;
-//   * small launches (< 1024 units, decode) add the residency cap below
-//     (256 decode tokens, plain / QK-normalized: 2.40 / 2.78 us with one item
-//     per thread in 192- / 64-thread CTAs and no cap, 2.07 / 2.57 us this way);
+//   * small launches (< 1024 units, decode) take up to 192 items per CTA --
+//     two 96-thread CTAs per Llama token -- and add the residency cap below.
+//     256 decode tokens, back to back: 2.15 -> 2.12 us (FP8 2.18 -> 2.15,
+//     slot mapping 2.30 -> 2.28, QK-normalized 2.48 either way) against one
+//     192-thread CTA per token; three 64-thread CTAs 2.14 us; one item per
+//     thread in two or three CTAs per token 2.39 us;
 //   * the large QK-normalized launch, ~3x the arithmetic per byte, keeps 32
 //     threads x 4 items per CTA (more loads in flight per thread; 96 x 4 with
 //     dependent launch: 31.60 us, the same), and the large FP8-cache launch
@@ -64,7 +67,10 @@ Shape pick_shape(int items, long long units, Work work = Work::kPlain)
     Shape sh;
     int perCta;
     sh.small = units < 1024;
-    if (sh.small || work == Work::kPlain) {
+    if (sh.small) {
+        sh.ipt = 2;
+        perCta = 192;
+    } else if (work == Work::kPlain) {
         sh.ipt = 2;
         perCta = 384;
     } else if (work == Work::kNorm) {

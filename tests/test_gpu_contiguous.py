@@ -223,11 +223,12 @@ def test_dependent_back_to_back_calls(B, S):
 @pytest.mark.parametrize("norm", [False, True])
 @pytest.mark.parametrize("cap_on", [True, False])
 def test_small_launch_residency_caps(tokens, norm, cap_on):
-    """Decode-sized launches (fewer than 1024 tokens) reserve dynamic shared
-    memory so that at most ceil(CTAs / SMs) CTAs share an SM: 1, 2, 3, 4, 5
-    and 7 CTAs per SM here (the normalized call, two CTAs per token, also
-    crosses the 8-per-SM limit above which no memory is reserved). Every cap,
-    and the cap switched off by the caller, gives the oracle's result."""
+    """Decode-sized launches (fewer than 1024 tokens; two CTAs per token of
+    8 + 2 x 2 heads here) reserve dynamic shared memory so that at most
+    ceil(CTAs / SMs) CTAs share an SM: 1, 2, 3, 6 and 8 CTAs per SM here, and
+    609 tokens and more cross the 8-per-SM limit above which no memory is
+    reserved. Every cap, and the cap switched off by the caller, gives the
+    oracle's result."""
     import rope_kv_cache_gb300 as rk
     case = workloads.make_continuous(tokens, 1, 8, 2, 128, 128, 16, NEOX, 5e5, seed=4000 + tokens,
                                      name=f"caps{tokens}")

@@ -510,10 +510,11 @@ def make_slotmap(seq_lens, Hq, Hkv, D, r, style, theta, seed, block_size, num_bl
 
 CONFIG_NAMES = ("packed_tiny", "prefill", "decode", "tree", "paged")
 
-# Smaller-footprint twins of two workloads for profiler captures: the same
+# Smaller-footprint twins of workloads for profiler captures: the same
 # tokens / rows per launch, a smaller cache (decode: capacity 1024) or pool
 # (paged: 64 logical pages per sequence, 8192 pages per plane, positions < 4096).
-PROFILE_NAMES = ("decode_c1024", "paged_p8192", "paged_fused_p8192", "slotmap_prefill_b4096")
+PROFILE_NAMES = ("decode_c1024", "decode_qknorm_c1024", "decode_fp8_c1024", "paged_p8192",
+                 "paged_fused_p8192", "slotmap_prefill_b4096", "slotmap_decode_b4096")
 
 # Workloads of the next rows (built on the same kernels).
 NEXT_NAMES = ("paged_fused", "slotmap_prefill", "slotmap_decode", "prefill_qknorm",
@@ -552,6 +553,18 @@ def config(name: str):
         cos_sin = cos_sin_table(5e5, 1024, 128)
         return ContiguousCase("continuous", 256, 1, 32, 8, 128, 128, 1024, NEOX, 5e5, cos_sin,
                               qkv, end_lens=end_lens, name=name)
+    if name in ("decode_qknorm_c1024", "decode_fp8_c1024"):
+        # profiler-sized twins of decode_qknorm / decode_fp8 (capacity 1024)
+        case = config("decode_c1024")
+        if name.startswith("decode_qknorm"):
+            case.norm = norm_weights(8, case.D)
+        else:
+            case.fp8_scales = (0.05, 0.04)
+        case.name = name
+        return case
+    if name == "slotmap_decode_b4096":
+        return make_slotmap([1] * 256, 32, 8, 128, 128, NEOX, 5e5, seed=7, block_size=64,
+                            num_blocks=4096, start_range=(0, 8191), cs_rows=8192, name=name)
     if name == "paged_p8192":
         return make_paged(16384, 128, 8, 128, 128, 64, 64, 8192, NEOX, 5e5, seed=4,
                           valid_rows=15565, name=name)
