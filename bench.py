@@ -111,7 +111,8 @@ def measured_peak():
 def source_sha():
     import hashlib
     h = hashlib.sha256()
-    for rel in ("rope_kv_cache_gb300/csrc/ropekv_kernels.cuh", "rope_kv_cache_gb300/csrc/ropekv_api.cu"):
+    for rel in ("rope_kv_cache_gb300/csrc/ropekv_kernels.cuh", "rope_kv_cache_gb300/csrc/ropekv_api.cu",
+                "rope_kv_cache_gb300/csrc/ropekv_floor.cu"):
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
