@@ -621,6 +621,10 @@ int paged_kv_delta_update_fused(const uint16_t* kDelta, const uint16_t* vDelta,
     a.mpps = maxPagesPerSeq;
     a.tpp = tokensPerPage;
     a.deltaWidth = deltaWidth;
+    a.widthShift = -1;
+    for (int sh = 0; sh < 31; ++sh)
+        if ((1 << sh) == deltaWidth)
+            a.widthShift = sh;
     a.sourceRows = sourceRows;
     a.cacheCapacity = cacheCapacity;
     a.itemsPerRow = 2 * numKVHeads * (headDim / 16);

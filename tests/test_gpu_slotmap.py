@@ -110,3 +110,15 @@ def test_configs_full(name):
     for cache in (kc, vc):
         n = int((cache.view(torch.int16) != sent).sum().item())
         assert n == case.T * case.Hkv * D
+
+
+@pytest.mark.parametrize("idx", [5, 6])
+def test_small_launches_with_residency_cap_off(idx):
+    """The decode-sized slot-mapping launches give the same result with the
+    residency cap switched off by the caller."""
+    import rope_kv_cache_gb300 as rk
+    prev = rk.ropekv_set_residency_cap(False)
+    try:
+        test_small_cases(idx)
+    finally:
+        rk.ropekv_set_residency_cap(prev)
