@@ -549,13 +549,16 @@ def _oracle_base_name(name: str) -> str:
 
 
 class OracleUnits:
-    """A workload's inputs cut into oracle calls of about `chunk` tokens."""
+    """A workload's inputs cut into oracle calls of about `chunk` tokens.
+    Each call returns its outputs; `meta[k]` says what unit k covers (the
+    tests check the units against the oracle's call on the whole case)."""
 
-    def __init__(self, name: str, chunk: int = 128):
+    def __init__(self, name: str, chunk: int = 128, case=None):
         self.name = name
-        c = workloads.config(_oracle_base_name(name))
+        c = case if case is not None else workloads.config(_oracle_base_name(name))
         self.case = c
         self.calls = []          # (callable, tokens it processes)
+        self.meta = []
         if isinstance(c, workloads.PagedCase):
             kw, vw = c.plane_written()
             valid = kw | vw
@@ -566,24 +569,29 @@ class OracleUnits:
                         np.ascontiguousarray(c.positions[sl]),
                         np.ascontiguousarray(c.seq_ids[sl]))
                 self.calls.append((self._paged_call(args), int(valid[sl].sum())))
+                self.meta.append(("rows", sl.start, sl.stop - sl.start))
             self.units_total = c.valid_rows
         elif isinstance(c, workloads.PagedFusedCase):
             kw, vw = c.plane_written()
             valid = (kw | vw).reshape(c.B, c.W)
             for b in range(c.B):
                 self.calls.append((self._fused_call(b), int(valid[b].sum())))
+                self.meta.append(("sequence", b))
             self.units_total = c.valid_rows
         elif isinstance(c, workloads.SlotMapCase):
             for t0 in range(0, c.T, chunk):
                 n = min(c.T, t0 + chunk) - t0
                 self.calls.append((self._slotmap_call(t0, n), n))
+                self.meta.append(("tokens", t0, n))
             self.units_total = c.T
         else:
-            self._cache = (np.zeros((1, 2, c.Hkv, c.cap, c.D), dtype=np.uint8)
+            nb = c.B if c.mode == "packed" else 1   # the packed call runs whole
+            self._cache = (np.zeros((nb, 2, c.Hkv, c.cap, c.D), dtype=np.uint8)
                            if c.fp8_scales is not None else
-                           np.zeros((1, 2, c.Hkv, c.cap, c.D), dtype=np.uint16))
+                           np.zeros((nb, 2, c.Hkv, c.cap, c.D), dtype=np.uint16))
             if c.mode == "packed":
                 self.calls.append((self._packed_call(), c.tokens))
+                self.meta.append(("all",))
             else:
                 n = min(chunk, c.S)
                 self._qout = np.zeros((1, n, c.Hq, c.D), dtype=np.uint16)
@@ -591,6 +599,7 @@ class OracleUnits:
                     for s0 in range(0, c.S, n):
                         m = min(c.S, s0 + n) - s0
                         self.calls.append((self._contiguous_call(b, s0, m), m))
+                        self.meta.append(("chunk", b, s0, m))
             self.units_total = c.tokens
         self.bytes_per_unit = c.algorithmic_bytes() / max(1, self.units_total)
 
@@ -616,6 +625,7 @@ class OracleUnits:
                                       c.fp8_scales[1], c.Hq, c.Hkv, c.style)
             else:
                 oracle.continuous(c.cos_sin, end, qkv, cache, qout, c.Hq, c.Hkv, c.style)
+            return qout, cache
         return run
 
     def _packed_call(self):
@@ -625,6 +635,7 @@ class OracleUnits:
 
         def run():
             oracle.packed(c.cos_sin, qkv, self._cache, c.Hq, c.Hkv, c.style)
+            return qkv, self._cache
         return run
 
     def _paged_call(self, args):
@@ -633,8 +644,8 @@ class OracleUnits:
         k, v, cs, pos, seq = args
 
         def run():
-            oracle.paged_rows(k, v, cs, pos, seq, c.page_table, c.num_pages, c.tokens_per_page,
-                              c.style)
+            return oracle.paged_rows(k, v, cs, pos, seq, c.page_table, c.num_pages,
+                                     c.tokens_per_page, c.style)
         return run
 
     def _fused_call(self, b):
@@ -651,7 +662,8 @@ class OracleUnits:
         def run():
             pos, seq = oracle.delta_metadata(old, lens, W)
             cs = oracle.gather_delta_rope(c.source, pos, seq, state, 1)
-            oracle.paged_rows(k, v, cs, pos, seq, table, c.num_pages, c.tokens_per_page, c.style)
+            return oracle.paged_rows(k, v, cs, pos, seq, table, c.num_pages, c.tokens_per_page,
+                                     c.style)
         return run
 
     def _slotmap_call(self, t0, n):
@@ -669,6 +681,7 @@ class OracleUnits:
         def run():
             oracle.slot_mapping(c.cos_sin, pos, qkv[:, :Hq], qkv[:, Hq:Hq + Hkv],
                                 qkv[:, Hq + Hkv:], slots, kc, vc, qout, None, c.style)
+            return qout, kc, vc, slots
         return run
 
     def run_units(self, first: int, count: int = 0, budget_s: float = 0.0):
