@@ -87,7 +87,10 @@ Shape pick_shape(int items, long long units, Work work = Work::kPlain)
 }
 
 // Kernel policies (see ropekv_kernels.cuh), measured on GB300:
-//   * every launch: streaming L2 hints on activations and cache rows;
+//   * every launch: streaming L2 hints on activations and cache rows, and
+//     cos/sin rows kept in L2 (evict-last; against no hint: paged update 21.25
+//     -> 21.10 us, QK-normalized decode 2.47 -> 2.45 us, tree 16.04 -> 16.01,
+//     the others within 0.2 %);
 //   * small (decode-sized) token and slot-mapping launches: programmatic
 //     dependent launch with the L2 prefetch prologue, which takes the
 //     position -> cos/sin chain and the input reads off the critical path
@@ -103,9 +106,9 @@ Shape pick_shape(int items, long long units, Work work = Work::kPlain)
 //     short) launch without it (the fused update: 13.9 -> 17.3 us with it).
 // Kernels that do not wait on the previous grid (the DFlash metadata and
 // gather kernels) never get the dependent-launch attribute.
-constexpr int kPolLarge = ropekv::kStreamHint;
-constexpr int kPolPdl = ropekv::kStreamHint | ropekv::kPdl;
-constexpr int kPolSmall = ropekv::kStreamHint | ropekv::kPdl | ropekv::kPrefetch;
+constexpr int kPolLarge = ropekv::kStreamHint | ropekv::kTableKeep;
+constexpr int kPolPdl = ropekv::kStreamHint | ropekv::kTableKeep | ropekv::kPdl;
+constexpr int kPolSmall = ropekv::kStreamHint | ropekv::kTableKeep | ropekv::kPdl | ropekv::kPrefetch;
 constexpr long long kPdlMaxCtas = 12288;
 
 bool pdl_allowed(unsigned grid, const Shape& sh)

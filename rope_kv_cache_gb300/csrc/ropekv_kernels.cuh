@@ -123,8 +123,9 @@ struct GatherArgs {
 //                reads or writes anything: safe whatever that grid did.
 //   kStreamHint: activations and cache rows are touched once per call: load
 //                them bypassing L1 and mark loads and stores evict-first in L2.
-//   kTableKeep:  cos/sin rows are reused by every call: mark them evict-last
-//                in L2 so the streaming traffic does not push them out.
+//   kTableKeep:  cos/sin rows are reused across tokens and calls: mark them
+//                evict-last in L2 so the streaming traffic does not push
+//                them out.
 //   kPrefetch:   (with kPdl) before waiting for the previous grid, warm L2 with
 //                the thread's input vectors and the cos/sin row of the token's
 //                speculatively read position. Only L2 prefetches and
