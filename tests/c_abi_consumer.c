@@ -3,8 +3,8 @@
  * and sizes -- no Python, no torch.
  *
  *   c_abi_consumer host
- *       host-only calls: rope_check_capacity and ropekv_status_string; prints
- *       one line per result.
+ *       host-only calls: rope_check_capacity, ropekv_status_string and
+ *       ropekv_set_residency_cap; prints one line per result.
  *   c_abi_consumer packed B S Hq Hkv D r cap style cos_sin.bin qkv.bin out_qkv.bin out_cache.bin
  *       reads the FP32 cos/sin table [1, cap, r] and the FP16 qkv bits
  *       [B, S, Hq+2Hkv, D], runs rope_write_kv_packed on the device with a
@@ -55,6 +55,10 @@ static int run_host(void)
     printf("capacity(4097, 4096) = %d\n", rope_check_capacity(4097, 4096));
     for (int s = 0; s >= -10; --s)
         printf("status %d: %s\n", s, ropekv_status_string(s));
+    /* the residency-cap switch returns its previous setting (on by default) */
+    const int was = ropekv_set_residency_cap(0);
+    const int now = ropekv_set_residency_cap(was);
+    printf("residency cap: default %d, after switching off %d\n", was, now);
     return 0;
 }
 

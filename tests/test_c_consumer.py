@@ -42,7 +42,8 @@ def test_host_calls_from_c(consumer):
     assert lines[0] == "capacity(4096, 4096) = 0"
     assert lines[1] == "capacity(4097, 4096) = -8"        # ROPEKV_ERR_CAPACITY
     assert lines[2] == "status 0: ok"
-    assert len(lines) == 13 and all(line.startswith("status -") for line in lines[3:])
+    assert len(lines) == 14 and all(line.startswith("status -") for line in lines[3:13])
+    assert lines[13] == "residency cap: default 1, after switching off 0"
 
 
 @pytest.mark.gpu
