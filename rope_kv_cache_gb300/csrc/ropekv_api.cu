@@ -110,14 +110,6 @@ constexpr int kPolLarge = ropekv::kStreamHint | ropekv::kTableKeep;
 constexpr int kPolPdl = ropekv::kStreamHint | ropekv::kTableKeep | ropekv::kPdl;
 constexpr int kPolSmall = ropekv::kStreamHint | ropekv::kTableKeep | ropekv::kPdl | ropekv::kPrefetch;
 constexpr long long kPdlMaxCtas = 12288;
-// Large contiguous-cache launches whose sequences write at least this many
-// consecutive slots store the cache rows with normal L2 priority
-// (kCacheNormal). Measured on GB300: the prefill, 4 x 2048 tokens, 30.08 ->
-// 28.35 us per launch; 4096 tokens as 4096 / S sequences of S tokens, S = 128
-// ... 2048: 1 % ... 3.4 % faster; the FP8-cache and QK-normalized prefills
-// 1.4 % faster. Shorter runs keep evict-first: the tree's 64-token sequences
-// took 16.00 -> 16.27 us with normal priority, one-token decodes 6 % longer.
-constexpr int kCacheNormalMinTokens = 128;
 
 bool pdl_allowed(unsigned grid, const Shape& sh)
 {
@@ -220,18 +212,11 @@ int launch_token_variant(const TokenArgs& a, unsigned grid, const Shape& sh, cud
                 ropekv::rope_kv_token_kernel<D, STYLE, MODE, IPT, kPolSmall, NORM, FP8>>(
                 grid, sh.threads, st, a);
     }
-    using ropekv::rope_kv_token_kernel;
-    constexpr int kCN = ropekv::kCacheNormal;
-    const bool runs = a.S >= kCacheNormalMinTokens;
     if (pdl_allowed(grid, sh))
-        return runs ? launch_k(rope_kv_token_kernel<D, STYLE, MODE, IPT, kPolPdl | kCN, NORM, FP8>,
-                               grid, sh.threads, st, true, a)
-                    : launch_k(rope_kv_token_kernel<D, STYLE, MODE, IPT, kPolPdl, NORM, FP8>,
-                               grid, sh.threads, st, true, a);
-    return runs ? launch_k(rope_kv_token_kernel<D, STYLE, MODE, IPT, kPolLarge | kCN, NORM, FP8>,
-                           grid, sh.threads, st, false, a)
-                : launch_k(rope_kv_token_kernel<D, STYLE, MODE, IPT, kPolLarge, NORM, FP8>, grid,
-                           sh.threads, st, false, a);
+        return launch_k(ropekv::rope_kv_token_kernel<D, STYLE, MODE, IPT, kPolPdl, NORM, FP8>,
+                        grid, sh.threads, st, true, a);
+    return launch_k(ropekv::rope_kv_token_kernel<D, STYLE, MODE, IPT, kPolLarge, NORM, FP8>, grid,
+                    sh.threads, st, false, a);
 }
 
 template <int D, int STYLE, int MODE, int IPT>

@@ -126,18 +126,13 @@ struct GatherArgs {
 //   kTableKeep:  cos/sin rows are reused across tokens and calls: mark them
 //                evict-last in L2 so the streaming traffic does not push
 //                them out.
-//   kCacheNormal: (contiguous-cache kernel) K/V cache rows are stored with
-//                normal L2 priority instead of evict-first: a line stays in L2
-//                long enough for the rows of the following slots to join it,
-//                so its write-back reaches DRAM with its neighbours. Worth it
-//                when each sequence writes runs of consecutive slots.
 //   kPrefetch:   (with kPdl) before waiting for the previous grid, warm L2 with
 //                the thread's input vectors and the cos/sin row of the token's
 //                speculatively read position. Only L2 prefetches and
 //                L1-bypassing loads happen before the wait, so nothing stale can
 //                be consumed afterwards (L2 is the point of coherence), and a
 //                wrong speculative position only wastes one prefetch.
-enum Policy : int { kPdl = 1, kStreamHint = 2, kTableKeep = 4, kPrefetch = 8, kCacheNormal = 16 };
+enum Policy : int { kPdl = 1, kStreamHint = 2, kTableKeep = 4, kPrefetch = 8 };
 
 __device__ __forceinline__ void prefetch_l2(const void* p)
 {
@@ -155,19 +150,6 @@ struct L2Policies {
     uint64_t stream;
     uint64_t keep;
 };
-
-// The L2 policy of the contiguous-cache kernel's K/V cache stores.
-template <int POL>
-__device__ __forceinline__ L2Policies cache_store_policies(const L2Policies& pol)
-{
-    if constexpr ((POL & kCacheNormal) != 0) {
-        L2Policies c = pol;
-        asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(c.stream));
-        return c;
-    } else {
-        return pol;
-    }
-}
 
 template <int POL>
 __device__ __forceinline__ L2Policies make_policies()
@@ -600,7 +582,6 @@ __global__ void __launch_bounds__(256) rope_kv_token_kernel(const TokenArgs a)
     }
 
     // 4. rotate and store
-    const L2Policies cpol = cache_store_policies<POL>(pol);
     float invK = 1.0f, invV = 1.0f;
     if (FP8) {
         invK = 1.0f / __ldg(a.kScale);
@@ -629,8 +610,8 @@ __global__ void __launch_bounds__(256) rope_kv_token_kernel(const TokenArgs a)
             const int plane = isK ? 0 : 1;
             const int hk = isK ? head - a.Hq : head - a.Hq - a.Hkv;
             uint8_t* dst = a.cache8 + ((((size_t)b * 2 + plane) * a.Hkv + hk) * a.cap + slot) * D;
-            store_v8<POL>(dst + 8 * va, pack8_e4m3(fa), cpol);
-            store_v8<POL>(dst + 8 * vb, pack8_e4m3(fb), cpol);
+            store_v8<POL>(dst + 8 * va, pack8_e4m3(fa), pol);
+            store_v8<POL>(dst + 8 * vb, pack8_e4m3(fb), pol);
             continue;
         }
         uint16_t* dst;
@@ -653,9 +634,8 @@ __global__ void __launch_bounds__(256) rope_kv_token_kernel(const TokenArgs a)
             const int hv = head - a.Hq - a.Hkv;
             dst = a.cache + ((((size_t)b * 2 + 1) * a.Hkv + hv) * a.cap + slot) * D;
         }
-        const L2Policies& sp = head < a.Hq ? pol : cpol;  // qOut / in-place Q, or the cache
-        store_v<POL>(dst + 8 * va, xa[k], sp);
-        store_v<POL>(dst + 8 * vb, xb[k], sp);
+        store_v<POL>(dst + 8 * va, xa[k], pol);
+        store_v<POL>(dst + 8 * vb, xb[k], pol);
     }
 }
 
