@@ -44,6 +44,7 @@ EXTRA = ("decode", "decode_floor", "tree", "paged", "packed_tiny", "paged_fused"
          "slotmap_prefill", "slotmap_decode", "prefill_qknorm", "decode_qknorm", "prefill_fp8",
          "decode_fp8")
 NOMINAL_HBM_GBS = 8000.0
+CACHE_RING_BUDGET = 16 * 2 ** 30  # device bytes for one contiguous cache per ring set
 FALLBACK_HBM_GBS = 6800.0
 
 DESCR = {
@@ -263,15 +264,26 @@ class DeviceWorkload:
             if c.fp8_scales is not None:
                 self.fp8 = tuple(torch.tensor([v], dtype=torch.float32, device=device)
                                  for v in c.fp8_scales)
-                self.cache = torch.full((c.B, 2, c.Hkv, c.cap, c.D), workloads.SENTINEL8,
-                                        dtype=torch.uint8, device=device)
-            else:
-                self.cache = (t(c.new_cache()) if c.cache_init == "zero"
-                              else self._sentinel((c.B, 2, c.Hkv, c.cap, c.D)))
+
+            def new_cache():
+                if c.fp8_scales is not None:
+                    return torch.full((c.B, 2, c.Hkv, c.cap, c.D), workloads.SENTINEL8,
+                                      dtype=torch.uint8, device=device)
+                return (t(c.new_cache()) if c.cache_init == "zero"
+                        else self._sentinel((c.B, 2, c.Hkv, c.cap, c.D)))
+            # One cache per ring set where they fit, as the layers of a model
+            # each write their own: no step rewrites slots that the previous
+            # step left in L2. A shared cache (the 8.6 GB decode cache) is only
+            # used where the sets' slots almost never meet (one random slot per
+            # sequence).
+            cache_bytes = c.B * 2 * c.Hkv * c.cap * c.D * (1 if c.fp8_scales is not None else 2)
+            self.caches_per_set = self.ring * cache_bytes <= CACHE_RING_BUDGET
+            self.cache = new_cache()
             qkv_base = t(c.qkv)
             for k in range(self.ring):
                 end, pos = workloads.step_variant(c, k)
                 s = dict(qkv=qkv_base.clone() if k else qkv_base)
+                s["cache"] = new_cache() if (k and self.caches_per_set) else self.cache
                 if c.mode != "packed":
                     s["end"] = t(end)
                     s["qout"] = self._sentinel((c.B, c.S, c.Hq, c.D))
@@ -332,22 +344,22 @@ class DeviceWorkload:
             rk.paged_kv_delta_update(s["k"], s["v"], self.pool, s["cs"], s["pos"], s["seq"],
                                      s["pt"], style=c.style, stream=stream)
         elif c.mode == "packed":
-            rk.rope_write_kv_packed(self.cos_sin, s["qkv"], self.cache, c.Hq, c.Hkv, c.style,
+            rk.rope_write_kv_packed(self.cos_sin, s["qkv"], s["cache"], c.Hq, c.Hkv, c.style,
                                     stream=stream)
         elif c.mode == "tree":
-            rk.rope_write_kv_tree(self.cos_sin, s["end"], s["pos"], s["qkv"], self.cache,
+            rk.rope_write_kv_tree(self.cos_sin, s["end"], s["pos"], s["qkv"], s["cache"],
                                   s["qout"], c.Hq, c.Hkv, c.style, stream=stream)
         elif self.fp8 is not None:
-            rk.rope_write_kv_continuous_fp8(self.cos_sin, s["end"], s["qkv"], self.cache,
+            rk.rope_write_kv_continuous_fp8(self.cos_sin, s["end"], s["qkv"], s["cache"],
                                             s["qout"], self.fp8[0], self.fp8[1], c.Hq, c.Hkv,
                                             c.style, stream=stream)
         elif self.norm is not None:
             qw, kw, eps = self.norm
-            rk.rope_write_kv_continuous_qknorm(self.cos_sin, s["end"], s["qkv"], self.cache,
+            rk.rope_write_kv_continuous_qknorm(self.cos_sin, s["end"], s["qkv"], s["cache"],
                                                s["qout"], qw, kw, eps, c.Hq, c.Hkv, c.style,
                                                stream=stream)
         else:
-            rk.rope_write_kv_continuous(self.cos_sin, s["end"], s["qkv"], self.cache, s["qout"],
+            rk.rope_write_kv_continuous(self.cos_sin, s["end"], s["qkv"], s["cache"], s["qout"],
                                         c.Hq, c.Hkv, c.style, stream=stream)
 
 
@@ -871,6 +883,7 @@ def main(argv=None):
             wl.paged or wl.fused or wl.slotmap or wl.case.norm is not None
             or wl.case.fp8_scales is not None) else None
     tokens, bytes_step, ring = wl.tokens, wl.bytes, wl.ring
+    per_set = getattr(wl, "caches_per_set", None)
     kernel = _kernel_name(wl)
     del wl
     torch.cuda.empty_cache()
@@ -891,6 +904,7 @@ def main(argv=None):
                             "effective_gbs": gbs, "frac_of_measured_peak": gbs / peak,
                             "frac_of_nominal_8tbs": gbs / NOMINAL_HBM_GBS,
                             "launches_timed": args.extra_steps, "kernel": _kernel_name(w),
+                            "cache_per_ring_set": getattr(w, "caches_per_set", None),
                             "dram_bytes_per_launch_ncu": ncu_traffic(xname)}
             del w
             torch.cuda.empty_cache()
@@ -950,7 +964,10 @@ def main(argv=None):
                    "bytes_per_step": bytes_step,
                    "parallelism": f"one independent replica per GPU x{world} (no exchange)",
                    "l2": f"inputs larger than L2: ring of {ring} input sets, "
-                         f"{ring * bytes_step / 1e6:.0f} MB > 2 x L2 ({l2 / 1e6:.0f} MB)"},
+                         f"{ring * bytes_step / 1e6:.0f} MB > 2 x L2 ({l2 / 1e6:.0f} MB)",
+                   "caches": None if per_set is None else
+                   ("one KV cache per ring set (each step writes a cache the previous step did "
+                    "not)" if per_set else "one KV cache shared by the ring sets")},
         "effective_gbs": achieved,
         "pct_of_peak": {"measured_copy": 100 * achieved / peak,
                         "nominal_8tbs": 100 * achieved / NOMINAL_HBM_GBS},
