@@ -43,10 +43,10 @@
  *   - Return value: ROPEKV_OK (0), or a negative ropekv_status when the host
  *     rejected the arguments (nothing launched) or the launch failed. A
  *     launch failure is read from that launch's own result
- *     (cudaLaunchKernelEx); the library never calls cudaGetLastError on a
- *     launch path, so it neither reports nor clears an error that the caller
- *     left pending. (An error that earlier work left in the context can still
- *     make the launch itself fail.)
+ *     (cudaLaunchKernelEx); the library never calls cudaGetLastError or
+ *     cudaPeekAtLastError, so it neither reports nor clears an error that the
+ *     caller left pending. (An error that earlier work left in the context can
+ *     still make the launch itself fail.)
  *     Data-dependent invalid indices found on the device (negative or
  *     out-of-range positions, sequences, slots or pages) are skipped: nothing
  *     is written for them, and no error is raised ([DRK] skip rules).

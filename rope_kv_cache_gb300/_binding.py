@@ -86,7 +86,7 @@ def load_library():
     return lib
 
 
-class _on:
+class _OnDevice:
     """The library's entry points, each called with ``device`` made the
     calling thread's current CUDA device for the duration of the call: a
     launch, and the residency cap of small launches, act on the current
@@ -125,7 +125,7 @@ def load_floor_library():
     return _floor_lib
 
 
-def ropekv_floor_copy(src: torch.Tensor, dst: torch.Tensor, threads_per_cta: int = 192,
+def ropekv_floor_copy(src: torch.Tensor, dst: torch.Tensor, threads_per_cta: int = 96,
                       cap: bool = True, stream: Optional[torch.cuda.Stream] = None) -> None:
     """Copy src to dst (same size, contiguous, on one device) with the launch
     shape and policy of the library's decode-sized launches
@@ -230,7 +230,7 @@ def rope_write_kv_packed(cos_sin: torch.Tensor, qkv: torch.Tensor, kv_cache: tor
     """
     dims = _contiguous_dims(cos_sin, qkv, kv_cache, num_q_heads, num_kv_heads, style)
     dev = qkv.device
-    rc = _on(dev).rope_write_kv_packed(
+    rc = _OnDevice(dev).rope_write_kv_packed(
         _dev_ptr(cos_sin, "cos_sin", _F32, dev), _dev_ptr(qkv, "qkv", _F16, dev),
         _dev_ptr(kv_cache, "kv_cache", _F16, dev), ctypes.byref(dims), _stream_handle(stream, dev))
     _check_rc("rope_write_kv_packed", rc)
@@ -247,7 +247,7 @@ def rope_write_kv_continuous(cos_sin: torch.Tensor, kv_cache_end_lens: torch.Ten
     if tuple(kv_cache_end_lens.shape) != (B,) or tuple(q_out.shape) != (B, S, num_q_heads, D):
         raise ValueError("kv_cache_end_lens [B] and q_out [B,S,Hq,D] expected")
     dev = qkv.device
-    rc = _on(dev).rope_write_kv_continuous(
+    rc = _OnDevice(dev).rope_write_kv_continuous(
         _dev_ptr(cos_sin, "cos_sin", _F32, dev),
         _dev_ptr(kv_cache_end_lens, "kv_cache_end_lens", _I32, dev),
         _dev_ptr(qkv, "qkv", _F16, dev), _dev_ptr(kv_cache, "kv_cache", _F16, dev),
@@ -269,7 +269,7 @@ def rope_write_kv_continuous_qknorm(cos_sin: torch.Tensor, kv_cache_end_lens: to
             or tuple(q_norm_weight.shape) != (D,) or tuple(k_norm_weight.shape) != (D,):
         raise ValueError("kv_cache_end_lens [B], q_out [B,S,Hq,D], norm weights [D] expected")
     dev = qkv.device
-    rc = _on(dev).rope_write_kv_continuous_qknorm(
+    rc = _OnDevice(dev).rope_write_kv_continuous_qknorm(
         _dev_ptr(cos_sin, "cos_sin", _F32, dev),
         _dev_ptr(kv_cache_end_lens, "kv_cache_end_lens", _I32, dev),
         _dev_ptr(qkv, "qkv", _F16, dev), _dev_ptr(kv_cache, "kv_cache", _F16, dev),
@@ -295,7 +295,7 @@ def rope_write_kv_continuous_fp8(cos_sin: torch.Tensor, kv_cache_end_lens: torch
             or k_scale.numel() != 1 or v_scale.numel() != 1:
         raise ValueError("kv_cache_end_lens [B], q_out [B,S,Hq,D], one-element scales expected")
     dev = qkv.device
-    rc = _on(dev).rope_write_kv_continuous_fp8(
+    rc = _OnDevice(dev).rope_write_kv_continuous_fp8(
         _dev_ptr(cos_sin, "cos_sin", _F32, dev),
         _dev_ptr(kv_cache_end_lens, "kv_cache_end_lens", _I32, dev),
         _dev_ptr(qkv, "qkv", _F16, dev), _dev_ptr(kv_cache, "kv_cache", _U8, dev),
@@ -316,7 +316,7 @@ def rope_write_kv_tree(cos_sin: torch.Tensor, kv_cache_end_lens: torch.Tensor,
             or tuple(q_out.shape) != (B, S, num_q_heads, D):
         raise ValueError("kv_cache_end_lens [B], token_pos_ids [B,S], q_out [B,S,Hq,D] expected")
     dev = qkv.device
-    rc = _on(dev).rope_write_kv_tree(
+    rc = _OnDevice(dev).rope_write_kv_tree(
         _dev_ptr(cos_sin, "cos_sin", _F32, dev),
         _dev_ptr(kv_cache_end_lens, "kv_cache_end_lens", _I32, dev),
         _dev_ptr(token_pos_ids, "token_pos_ids", _I32, dev),
@@ -350,7 +350,7 @@ def paged_kv_delta_update(k_delta: torch.Tensor, v_delta: torch.Tensor, kv_cache
     if batch_size > B:
         raise ValueError("batch_size exceeds the page table's rows")
     dev = k_delta.device
-    rc = _on(dev).paged_kv_delta_update(
+    rc = _OnDevice(dev).paged_kv_delta_update(
         _dev_ptr(k_delta, "k_delta", _F16, dev), _dev_ptr(v_delta, "v_delta", _F16, dev),
         _dev_ptr(kv_cache, "kv_cache", _F16, dev),
         _dev_ptr(token_aligned_cos_sin, "token_aligned_cos_sin", _F32, dev),
@@ -391,7 +391,7 @@ def paged_kv_delta_update_fused(k_delta: torch.Tensor, v_delta: torch.Tensor,
             or (state_indices is not None and tuple(state_indices.shape) != (B,)):
         raise ValueError("inconsistent shapes for paged_kv_delta_update_fused")
     dev = k_delta.device
-    rc = _on(dev).paged_kv_delta_update_fused(
+    rc = _OnDevice(dev).paged_kv_delta_update_fused(
         _dev_ptr(k_delta, "k_delta", _F16, dev), _dev_ptr(v_delta, "v_delta", _F16, dev),
         _dev_ptr(kv_cache, "kv_cache", _F16, dev),
         _dev_ptr(cos_sin_source, "cos_sin_source", _F32, dev),
@@ -415,7 +415,7 @@ def dflash_prepare_delta_metadata(old_draft_cache_lengths: torch.Tensor,
             or delta_token_to_sequence.numel() != B * delta_width:
         raise ValueError("inconsistent shapes for dflash_prepare_delta_metadata")
     dev = old_draft_cache_lengths.device
-    rc = _on(dev).dflash_prepare_delta_metadata(
+    rc = _OnDevice(dev).dflash_prepare_delta_metadata(
         _dev_ptr(old_draft_cache_lengths, "old_draft_cache_lengths", _I32, dev),
         _dev_ptr(delta_lengths, "delta_lengths", _I32, dev), int(delta_width),
         _dev_ptr(delta_positions, "delta_positions", _I32, dev),
@@ -441,7 +441,7 @@ def dflash_gather_delta_rope(source: torch.Tensor, output: torch.Tensor,
     if batch_size is None:
         batch_size = state_indices.shape[0] if state_indices is not None else N
     dev = output.device
-    rc = _on(dev).dflash_gather_delta_rope(
+    rc = _OnDevice(dev).dflash_gather_delta_rope(
         _dev_ptr(source, "source", _F32, dev), _dev_ptr(output, "output", _F32, dev),
         _dev_ptr(delta_positions, "delta_positions", _I32, dev),
         _dev_ptr(delta_token_to_sequence, "delta_token_to_sequence", _I32, dev),
@@ -473,7 +473,7 @@ def rope_write_kv_slot_mapping(cos_sin: torch.Tensor, positions: torch.Tensor, q
     qp, qs = _dev_rows(q, "q", dev)
     kp, ks = _dev_rows(k, "k", dev)
     vp, vs = _dev_rows(v, "v", dev)
-    rc = _on(dev).rope_write_kv_slot_mapping(
+    rc = _OnDevice(dev).rope_write_kv_slot_mapping(
         _dev_ptr(cos_sin, "cos_sin", _F32, dev), _dev_ptr(positions, "positions", _I64, dev),
         qp, qs, kp, ks, vp, vs, _dev_ptr(slot_mapping, "slot_mapping", _I64, dev),
         _dev_ptr(key_cache, "key_cache", _F16, dev), _dev_ptr(value_cache, "value_cache", _F16, dev),

@@ -147,8 +147,7 @@ std::atomic<int> g_residency_cap{1};
 // so that at most ceil(grid / SMs) CTAs fit on one SM, spreads the CTAs over
 // the GPU (256 decode tokens: 2.40 -> 2.07 us per launch). Returns 0 (no cap)
 // for grids of more than 8 CTAs per SM, when the caller switched the cap off
-// or when the device cannot be queried (a failed query's error is consumed
-// here: it is this function's own, and the launch then goes ahead uncapped);
+// or when the device cannot be queried (the launch then goes ahead uncapped);
 // *optin receives the device's per-block shared memory limit.
 size_t residency_smem(unsigned grid, int* optin)
 {
@@ -164,7 +163,6 @@ size_t residency_smem(unsigned grid, int* optin)
             cudaSuccess ||
         cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) !=
             cudaSuccess || sms <= 0) {
-        (void)cudaGetLastError();
         return 0;
     }
     const unsigned cap = (grid + (unsigned)sms - 1) / (unsigned)sms;
@@ -195,7 +193,6 @@ int launch_small(unsigned grid, int threads, cudaStream_t st, const Args& a)
                 cudaSuccess) {
                 raised.fetch_or(bit, std::memory_order_relaxed);
             } else {
-                (void)cudaGetLastError();  // this call's own error, handled here
                 smem = 0;  // launch without the cap rather than fail
             }
         }

@@ -56,8 +56,7 @@ size_t cap_smem(unsigned grid, int* optin)
             cudaSuccess ||
         cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) !=
             cudaSuccess || sms <= 0) {
-        (void)cudaGetLastError();  // this query's own error; launch uncapped
-        return 0;
+        return 0;  // launch uncapped
     }
     const unsigned per = (grid + (unsigned)sms - 1) / (unsigned)sms;
     if (per == 0 || per > 8)
@@ -98,8 +97,7 @@ extern "C" int ropekv_floor_copy(const void* src, void* dst, int64_t bytes, int3
                     cudaSuccess) {
                     raised.fetch_or(bit, std::memory_order_relaxed);
                 } else {
-                    (void)cudaGetLastError();  // this call's own error; launch uncapped
-                    smem = 0;
+                    smem = 0;  // launch uncapped
                 }
             }
         }
