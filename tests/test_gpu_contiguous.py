@@ -373,3 +373,21 @@ print("ok")
     r = subprocess.run([sys.executable, "-c", code], cwd=root, capture_output=True, text=True,
                        timeout=600)
     assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout + r.stderr
+
+
+@pytest.mark.parametrize("layout", ["one_token_sequences", "short_tree_sequences",
+                                    "qknorm_one_token"])
+def test_large_launches_of_short_sequences(layout):
+    """Launches of 1024 tokens and more take the large-launch path whatever
+    the sequences look like: 1536 one-token sequences (a large decode batch)
+    and 96 tree sequences of 16 tokens, on every element against the oracle
+    (small caches keep the oracle quick)."""
+    if layout == "short_tree_sequences":
+        case = workloads.make_tree(96, 16, 8, 2, 128, 64, 64, GPTJ, 1e4, seed=71,
+                                   base_range=(0, 40), name=layout)
+    else:
+        case = workloads.make_continuous(1536, 1, 8, 2, 128, 128, 16, NEOX, 5e5, seed=72,
+                                         name=layout)
+        if layout == "qknorm_one_token":
+            case.norm = workloads.norm_weights(72, 128)
+    check_contiguous(case)
