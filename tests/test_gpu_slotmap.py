@@ -122,3 +122,37 @@ def test_small_launches_with_residency_cap_off(idx):
         test_small_cases(idx)
     finally:
         rk.ropekv_set_residency_cap(prev)
+
+
+@pytest.mark.parametrize("T", [37, 1500])
+def test_three_different_token_strides(T):
+    """q, k and v each with a token stride of its own: q a view of a row padded
+    by three heads, k a plain tensor, v a view of a row padded by one head (and
+    starting one head in), against the oracle on the same views."""
+    import oracle
+    import rope_kv_cache_gb300 as rk
+    Hq, Hkv, D, r, bsz, nb = 8, 2, 128, 64, 16, (T + 15) // 16 + 2
+    rng = workloads.rng_for(4242 + T)
+    qbuf = workloads.fp16_normal(rng, (T, Hq + 3, D))
+    kbuf = workloads.fp16_normal(rng, (T, Hkv, D))
+    vbuf = workloads.fp16_normal(rng, (T, Hkv + 1, D))
+    q, k, v = qbuf[:, :Hq], kbuf, vbuf[:, 1:]
+    positions = rng.integers(0, 1024, size=T).astype(np.int64)
+    slots = rng.permutation(nb * bsz)[:T].astype(np.int64)
+    slots[::9] = -1
+    cs = workloads.cos_sin_table(1e4, 1024, r)[0]
+    dq, dk, dv = to_dev(qbuf), to_dev(kbuf), to_dev(vbuf)
+    gq, gk, gv = dq[:, :Hq], dk, dv[:, 1:]
+    assert len({gq.stride(0), gk.stride(0), gv.stride(0)}) == 3
+    kc, vc = dev_sentinel((nb, bsz, Hkv, D)), dev_sentinel((nb, bsz, Hkv, D))
+    qo, ko = dev_sentinel((T, Hq, D)), dev_sentinel((T, Hkv, D))
+    rk.rope_write_kv_slot_mapping(to_dev(cs), to_dev(positions), gq, gk, gv, to_dev(slots), kc,
+                                  vc, qo, ko, style=GPTJ)
+    torch.cuda.synchronize()
+    o_kc, o_vc = workloads.sentinel_fill((nb, bsz, Hkv, D)), workloads.sentinel_fill((nb, bsz, Hkv, D))
+    o_qo, o_ko = workloads.sentinel_fill((T, Hq, D)), workloads.sentinel_fill((T, Hkv, D))
+    oracle.slot_mapping(cs, positions, q, k, v, slots, o_kc, o_vc, o_qo, o_ko, GPTJ)
+    compare(to_host_bits(kc), o_kc, _rot_mask(D, r, True), "keyCache")
+    compare(to_host_bits(vc), o_vc, _rot_mask(D, r, False), "valueCache")
+    compare(to_host_bits(qo), o_qo, (np.arange(D) < r)[None, None, :], "qOut")
+    compare(to_host_bits(ko), o_ko, (np.arange(D) < r)[None, None, :], "kOut")

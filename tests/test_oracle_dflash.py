@@ -87,3 +87,17 @@ def test_fused_is_the_composition(style):
     # sequence 4 has no source row: its K is rotated by a zero row (zeros),
     # its V is still written
     assert (seq == 4).sum() == 1
+
+
+def test_gather_sequence_past_batch_is_zero_even_with_a_valid_state():
+    """A row whose sequence is not below batchSize has no state index to read
+    (stateIndices has batchSize entries), so its row is zero even where
+    stateIndices' memory past the batch would name a valid state row."""
+    pos = np.array([1, 2, 3], dtype=np.int32)
+    seq = np.array([0, 1, 2], dtype=np.int32)
+    states = np.array([1, 0, 1], dtype=np.int32)   # entry 2 lies past batchSize = 2
+    out = oracle.gather_delta_rope(_source(), pos, seq, states, batch_size=2)
+    assert out.tolist() == [[110, 111, 112, 113], [20, 21, 22, 23], [0, 0, 0, 0]]
+    three = np.concatenate([_source(), _source()[:1] + 1000])   # sourceRows 3 > batchSize
+    out = oracle.gather_delta_rope(three, pos, seq, None, batch_size=2)
+    assert out[2].tolist() == [0, 0, 0, 0] and out[1].tolist() == [120, 121, 122, 123]

@@ -391,3 +391,106 @@ def test_tree_position_at_table_end_is_skipped(style):
     _check_cache(cache, qkv, expect, {}, r, style, False)
     assert np.all(qout[0, 1] == SENT)
     assert np.array_equal(qout[0, 0], qkv[0, 0, :2]) and np.array_equal(qout[0, 2], qkv[0, 2, :2])
+
+
+# ------------------------------------------------------ argument checks --
+
+def _dims_case(B=2, S=2, Hq=2, Hkv=1, D=16, r=16, cs_batch=1, cap=4):
+    qkv = coded_qkv(B, S, Hq + 2 * Hkv, D)
+    cs = np.zeros((cs_batch, cap, r), dtype=np.float32)
+    cs[:, :, : r // 2] = 1.0
+    return (qkv, cs, np.full(B, S, np.int32), workloads.sentinel_fill((B, 2, Hkv, cap, D)),
+            workloads.sentinel_fill((B, S, Hq, D)))
+
+
+def _call(mode, qkv, cs, end, cache, qo, Hq, Hkv):
+    B, S = qkv.shape[:2]
+    D = qkv.shape[3]
+    if mode == "packed":
+        oracle.packed(cs, qkv, cache, Hq, Hkv, oracle.NEOX)
+    elif mode == "continuous":
+        oracle.continuous(cs, end, qkv, cache, qo, Hq, Hkv, oracle.NEOX)
+    elif mode == "tree":
+        pos = np.tile(np.arange(S, dtype=np.int32), (B, 1))
+        oracle.tree(cs, end, pos, qkv, cache, qo, Hq, Hkv, oracle.NEOX)
+    elif mode == "qknorm":
+        w = f16(np.ones(D))
+        oracle.continuous_qknorm(cs, end, qkv, cache, qo, w, w, 1e-6, Hq, Hkv, oracle.NEOX)
+    else:
+        c8 = np.zeros(cache.shape, dtype=np.uint8)
+        oracle.continuous_fp8(cs, end, qkv, c8, qo, 1.0, 1.0, Hq, Hkv, oracle.NEOX)
+
+
+@pytest.mark.parametrize("mode", ["packed", "continuous", "tree", "qknorm", "fp8"])
+@pytest.mark.parametrize("bad", ["cos_sin_batch", "gqa_ratio", "odd_rotary_dim"])
+def test_invalid_dims_are_rejected(mode, bad):
+    """The table batch is 1 (shared) or B (one table per sequence), nothing
+    else ("Apply Rope Write KV", cosSinCacheBatchSize); Q heads come in whole
+    groups per KV head (sglang rope_cache.py, QH_PER_KH = qh // kh); the
+    rotated dims form pairs. Each violation is an error that writes nothing,
+    while the same call with valid dims succeeds."""
+    Hq, Hkv, r, csb = 2, 1, 16, 1
+    if bad == "cos_sin_batch":
+        csb = 3                                    # B = 2
+    elif bad == "gqa_ratio":
+        Hq, Hkv = 3, 2
+    else:
+        r = 15
+    qkv, cs, end, cache, qo = _dims_case(Hq=Hq, Hkv=Hkv, r=r, cs_batch=csb)
+    with pytest.raises(ValueError):
+        _call(mode, qkv, cs, end, cache, qo, Hq, Hkv)
+    assert np.all(cache == SENT) and np.all(qo == SENT)
+    assert np.array_equal(qkv, coded_qkv(2, 2, Hq + 2 * Hkv, 16))
+    good = _dims_case(cs_batch=2)                 # batch of tables == B is valid
+    _call(mode, *good, 2, 1)
+
+
+def test_paged_plane_boundaries():
+    """Canonical page ids are flat indices of the [2, numPages] pool ("Dflash
+    Runtime Kernels", launchDFlashTargetKVCacheUpdate): a K write needs
+    0 <= id < numPages, a V write numPages <= id < 2 * numPages, each plane
+    decided on its own. numPages = 4, TPP = 4, one sequence, rows t at
+    positions 1, 6, 11, 12 (logical pages 0..3):
+
+        logical page   0   1   2   3
+        K column       4   3   0  -1    (4 == numPages is a V-plane id)
+        V column       5   7   8   3    (8 == 2 * numPages; 3 is a K-plane id)
+
+    Logical page 0's K id, read as a flat index, is V-plane page 0, which no
+    row writes: a K write there would show.
+    """
+    Hkv, D, r = 1, 16, 16
+    table = np.array([[[4, 3, 0, -1], [5, 7, 8, 3]]], dtype=np.int32)
+    positions = np.array([1, 6, 11, 12], dtype=np.int32)
+    seqs = np.zeros(4, dtype=np.int32)
+    t, d = np.meshgrid(np.arange(4), np.arange(D), indexing="ij")
+    k = f16(1 + d + 17 * t)[:, None, :]
+    v = f16(200 + d + 17 * t)[:, None, :]
+    cs = np.zeros((4, r), dtype=np.float32)
+    for i in range(4):
+        cs[i, r // 2:] = 2.0 ** i
+    pool = workloads.sentinel_fill((2, 4, 4, Hkv, D))
+    oracle.paged(np.ascontiguousarray(k), np.ascontiguousarray(v), pool, cs, positions, seqs,
+                 table, oracle.NEOX)
+    want_k = {(0, 3, 2): 1, (0, 0, 3): 2}           # (plane, page, slot) <- row
+    want_v = {(1, 1, 1): 0, (1, 3, 2): 1}
+    written = np.zeros(pool.shape[:3], dtype=bool)
+    for (pl, pg, sl), i in want_k.items():
+        written[pl, pg, sl] = True
+        assert np.array_equal(val(pool[pl, pg, sl, 0]), rotated_scaled(val(k[i, 0]), r, oracle.NEOX, i))
+    for (pl, pg, sl), i in want_v.items():
+        written[pl, pg, sl] = True
+        assert np.array_equal(pool[pl, pg, sl, 0], v[i, 0])
+    assert np.all(pool[~written] == SENT)
+
+
+def test_packed_rejects_table_shorter_than_sequence():
+    """The packed call's positions are 0 .. S-1 ("from the start positions"),
+    so a table with fewer than S rows cannot serve it: an error that writes
+    nothing, even though the cache is long enough."""
+    qkv = coded_qkv(1, 5, 4, 16)
+    cache = workloads.sentinel_fill((1, 2, 1, 8, 16))
+    with pytest.raises(ValueError):
+        oracle.packed(identity_table(4, 16), qkv, cache, 2, 1, oracle.NEOX)
+    assert np.all(cache == SENT) and np.array_equal(qkv, coded_qkv(1, 5, 4, 16))
+    oracle.packed(identity_table(5, 16), qkv, cache, 2, 1, oracle.NEOX)

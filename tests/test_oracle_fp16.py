@@ -81,3 +81,12 @@ def test_rne_matches_numpy_on_hard_doubles():
 ])
 def test_rne_closed_forms(x, bits):
     assert oracle.f64_to_f16(x) == bits
+
+
+def test_nan_encodes_as_a_quiet_nan_like_numpy():
+    # IEEE 754 arithmetic delivers quiet NaNs (top fraction bit set); the sign
+    # is kept. numpy's conversion gives the same patterns.
+    for x in (float("nan"), -float("nan")):
+        bits = oracle.f64_to_f16(x)
+        assert bits == int(_np_f16_bits(np.array([x]))[0])
+        assert bits & 0x7E00 == 0x7E00 and (bits >> 15) == int(math.copysign(1, x) < 0)

@@ -140,3 +140,46 @@ def test_fp8_position_past_table_is_skipped():
     assert np.all(q8[0, 2] == workloads.SENTINEL) and np.all(c8[0, :, 0, 5] == 0x7F)
     assert np.all(c8[0, :, 0, 3:5] == oracle.f64_to_e4m3(0.5))
     assert np.all(c8[0, :, 0, :3] == 0x7F) and np.all(c8[0, :, 0, 6:] == 0x7F)
+
+
+def test_fp8_k_rounds_once_from_the_rotation():
+    """sglang rope_cache.py Stage 3.2-3.4: the rotated K stays in the RoPE's
+    working precision, is multiplied by 1 / k_scale and is rounded once, to the
+    cache type; the FP16 rounding belongs only to the k_out/qOut copy. A row
+    with cos = 1 + 2^-12 and sin = 0 turns 1.0625 (an E4M3 tie between 1.0 and
+    1.125) into 1.0625 + 2^-12 * 1.0625: rounded directly that is 1.125
+    (0x39); through FP16 it would first fall back to the tie 1.0625 and then to
+    the even 1.0 (0x38)."""
+    D = r = 16
+    qkv = np.zeros((1, 1, 3, D), dtype=np.float16)
+    qkv[0, 0, :2, 0] = 1.0625                              # the Q head and the K head
+    cs = np.zeros((1, 1, r), dtype=np.float32)
+    cs[0, 0, : r // 2] = np.float32(1.0 + 2.0 ** -12)
+    c8 = np.zeros((1, 2, 1, 1, D), dtype=np.uint8)
+    q8 = workloads.sentinel_fill((1, 1, 1, D))
+    oracle.continuous_fp8(cs, np.array([1], dtype=np.int32), qkv.view(np.uint16), c8, q8, 1.0,
+                          1.0, 1, 1, oracle.NEOX)
+    assert c8[0, 0, 0, 0, 0] == 0x39
+    assert q8[0, 0, 0, 0] == 0x3C40                        # FP16 1.0625
+    assert oracle.f64_to_e4m3(1.0625) == 0x38              # the tie alone goes to even
+
+
+def test_fp8_scale_covers_the_whole_k_head():
+    """Stage 3.3 scales the whole K head vector (the kernel's head block is the
+    full head width) by 1 / k_scale, so with rotaryDim < headDim the dims past
+    rotaryDim are scaled too. Position 0 (identity row), k_scale 0.5: every K
+    element e becomes E4M3(2e); V scales by 1 / v_scale = 4."""
+    D, r = 32, 16
+    qkv = np.zeros((1, 1, 3, D))
+    qkv[0, 0, 1] = 1.0 + np.arange(D) / 16.0          # K head, exact in FP16
+    qkv[0, 0, 2] = 0.25
+    qkv = qkv.astype(np.float16).view(np.uint16)
+    cs = np.zeros((1, 1, r), dtype=np.float32)
+    cs[0, 0, : r // 2] = 1.0
+    c8 = np.zeros((1, 2, 1, 1, D), dtype=np.uint8)
+    q8 = workloads.sentinel_fill((1, 1, 1, D))
+    oracle.continuous_fp8(cs, np.array([1], dtype=np.int32), qkv, c8, q8, 0.5, 0.25, 1, 1,
+                          oracle.NEOX)
+    k = 1.0 + np.arange(D) / 16.0
+    assert [int(b) for b in c8[0, 0, 0, 0]] == [oracle.f64_to_e4m3(2 * e) for e in k]
+    assert np.all(c8[0, 1, 0, 0] == 0x38)              # 0.25 * 4 = 1.0

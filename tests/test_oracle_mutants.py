@@ -11,6 +11,7 @@ import shutil
 import subprocess
 import sys
 import tempfile
+from concurrent.futures import ThreadPoolExecutor
 
 import pytest
 
@@ -20,7 +21,7 @@ HDR = os.path.join(ROOT, "oracle", "ropekv_oracle.h")
 PIN_TESTS = ["tests/test_oracle_rope.py", "tests/test_oracle_entries.py",
              "tests/test_oracle_dflash.py", "tests/test_oracle_slotmap.py",
              "tests/test_oracle_qknorm.py", "tests/test_oracle_fp8.py",
-             "tests/test_oracle_fp16.py"]
+             "tests/test_oracle_fp16.py", "tests/test_oracle_cross_entry.py"]
 
 MUTANTS = {
     "neox_rotate_sign": ("out[d] = (d < h) ? -x[d + h] : x[d - h];",
@@ -86,21 +87,57 @@ MUTANTS = {
                                  "if (pos < 0 || slot < 0 || slot >= cap)"),
     "fp8_pos_upper_unchecked": ("if (slot < 0 || slot >= cap || slot >= csSeq)",
                                 "if (slot < 0 || slot >= cap)"),
+    "dims_cs_batch_unchecked": ("if (csBatch != 1 && csBatch != B)\n        return 0;", ""),
+    "dims_gqa_ratio_unchecked": ("if (Hq % Hkv != 0)\n        return 0;", ""),
+    "dims_odd_rotary_accepted": ("if (r <= 0 || r % 2 != 0 || r > D)\n        return 0;\n    if (csBatch",
+                                 "if (r <= 0 || r > D)\n        return 0;\n    if (csBatch"),
+    "f16_nan_signaling": ("return (uint16_t)(sign | 0x7E00u);", "return (uint16_t)(sign | 0x7C01u);"),
+    "fp8_k_rounded_through_f16": (
+        "kc[d] = ropekv_oracle_f64_to_e4m3(y[d] * (1.0 / (double)kScale));",
+        "kc[d] = ropekv_oracle_f64_to_e4m3(ropekv_oracle_f16_to_f64(ropekv_oracle_f64_to_f16(y[d])) * (1.0 / (double)kScale));"),
+    "fp8_v_uses_k_scale": ("(1.0 / (double)vScale));", "(1.0 / (double)kScale));"),
+    "gather_seq_upper_unchecked": ("int ok = pos >= 0 && seq >= 0 && seq < batchSize && pos < cacheCapacity;",
+                                   "int ok = pos >= 0 && seq >= 0 && pos < cacheCapacity;"),
+    "gather_invalid_row_not_zero": ("+ pos) * rotaryDim + d] : 0.0f;", "+ pos) * rotaryDim + d] : 1.0f;"),
+    "paged_k_plane_inclusive": ("if (idK >= 0 && idK < numPages) {", "if (idK >= 0 && idK <= numPages) {"),
+    "paged_v_plane_low_exclusive": ("if (idV >= numPages && (int64_t)idV < 2 * (int64_t)numPages)",
+                                    "if (idV > numPages && (int64_t)idV < 2 * (int64_t)numPages)"),
+    "paged_table_plane_major": (
+        "int32_t idK = pageTable[((size_t)seq * 2 + 0) * maxPagesPerSeq + lp];\n        int32_t idV = pageTable[((size_t)seq * 2 + 1) * maxPagesPerSeq + lp];",
+        "int32_t idK = pageTable[((size_t)0 * batchSize + seq) * maxPagesPerSeq + lp];\n        int32_t idV = pageTable[((size_t)1 * batchSize + seq) * maxPagesPerSeq + lp];"),
+    "metadata_sequence_is_row": ("deltaTokenToSequence[t] = b;", "deltaTokenToSequence[t] = j;"),
+    "rmsnorm_eps_not_passed": ("ropekv_oracle_rms_norm_f64(x, weight, eps, D, n);",
+                               "ropekv_oracle_rms_norm_f64(x, weight, 1e-6, D, n);"),
+    "slotmap_v_stride_ignored": ("memcpy(vc, v + (size_t)t * vStride", "memcpy(vc, v + (size_t)t * kStride"),
+    "slotmap_q_skipped_with_cache": (
+        "        const float* cs = cosSin + (size_t)pos * r;\n        for (int hq = 0; hq < Hq; ++hq)",
+        "        const float* cs = cosSin + (size_t)pos * r;\n        if (slotMapping[t] < 0)\n            continue;\n        for (int hq = 0; hq < Hq; ++hq)"),
+    "cache_plane_head_swapped": ("return ((((size_t)b * 2 + plane) * Hkv + hk) * (size_t)cap + slot) * (size_t)D;",
+                                 "return ((((size_t)b * Hkv + hk) * 2 + plane) * (size_t)cap + slot) * (size_t)D;"),
+    "tree_slot_from_position": ("long long slot = (long long)kvCacheEndLens[b] - S + s;\n            if (pos < 0",
+                                "long long slot = pos;\n            if (pos < 0"),
+    "fp8_tail_not_scaled": ("kc[d] = ropekv_oracle_f64_to_e4m3(y[d] * (1.0 / (double)kScale));",
+                            "kc[d] = ropekv_oracle_f64_to_e4m3(d < r ? y[d] * (1.0 / (double)kScale) : y[d]);"),
+    "packed_table_length_unchecked": ("if (S > cap || S > csSeq)", "if (S > cap)"),
+    "gather_source_transposed": ("source[((size_t)state * cacheCapacity + pos) * rotaryDim + d]",
+                                 "source[((size_t)pos * sourceRows + state) * rotaryDim + d]"),
+    "slotmap_cache_head_major": (
+        "uint16_t* kc = keyCache + (((size_t)block * blockSize + off) * Hkv + hk) * D;",
+        "uint16_t* kc = keyCache + (((size_t)block * Hkv + hk) * blockSize + off) * D;"),
+    "qknorm_norm_over_rotary_only": (
+        "ropekv_oracle_rms_norm_f64(x, weight, eps, D, n);",
+        "ropekv_oracle_rms_norm_f64(x, weight, eps, r, n);\n    for (int d = r; d < D; ++d)\n        n[d] = x[d] * ropekv_oracle_f16_to_f64(weight[d]);"),
+    "sin_index_mirrored": ("double s = (double)cs_row[h + f];", "double s = (double)cs_row[r - 1 - f];"),
 }
 
 
-@pytest.fixture(scope="module")
-def workdir():
-    d = tempfile.mkdtemp(prefix="ropekv_mutants_")
-    yield d
-    shutil.rmtree(d, ignore_errors=True)
-
-
-@pytest.mark.parametrize("name", sorted(MUTANTS))
-def test_mutant_is_caught(name, workdir):
+def _run_mutant(name, workdir):
+    """Build one mutant into its own library and run the pins against it in a
+    child process; returns (returncode, stdout)."""
     old, new = MUTANTS[name]
     src = open(SRC).read()
-    assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
+    if src.count(old) != 1:
+        return None, f"mutation site for {name} found {src.count(old)} times"
     mdir = os.path.join(workdir, name)
     os.makedirs(mdir, exist_ok=True)
     shutil.copy(HDR, mdir)
@@ -113,6 +150,27 @@ def test_mutant_is_caught(name, workdir):
     env = dict(os.environ, ROPEKV_ORACLE_LIB=lib)
     proc = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                            *PIN_TESTS], cwd=ROOT, env=env, capture_output=True, text=True,
-                          timeout=600)
-    assert proc.returncode != 0, f"mutant {name} passed every pin:\n{proc.stdout[-2000:]}"
-    assert "failed" in proc.stdout or "error" in proc.stdout.lower()
+                          timeout=900)
+    return proc.returncode, proc.stdout
+
+
+@pytest.fixture(scope="module")
+def results():
+    """Every mutant's pin run, side by side (each is an independent child
+    process on its own copy of the oracle)."""
+    d = tempfile.mkdtemp(prefix="ropekv_mutants_")
+    try:
+        workers = max(1, min(8, os.cpu_count() or 1))
+        with ThreadPoolExecutor(workers) as ex:
+            futs = {n: ex.submit(_run_mutant, n, d) for n in MUTANTS}
+            yield {n: f.result() for n, f in futs.items()}
+    finally:
+        shutil.rmtree(d, ignore_errors=True)
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, results):
+    rc, out = results[name]
+    assert rc is not None, out
+    assert rc != 0, f"mutant {name} passed every pin:\n{out[-2000:]}"
+    assert "failed" in out or "error" in out.lower()

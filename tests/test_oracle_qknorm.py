@@ -139,3 +139,26 @@ def test_qknorm_position_past_table_is_skipped():
     assert np.all(qo[0, 2] == workloads.SENTINEL) and np.all(cache[0, :, 0, 5] == workloads.SENTINEL)
     assert np.all(qo[0, :2].view(np.float16) == 1.0)
     assert np.all(cache[0, 0, 0, 3:5].view(np.float16) == 1.0)
+
+
+def test_entry_point_applies_its_eps():
+    """The call's eps enters the RMS denominator (libmir-cuda execution.rs,
+    qkv_postprocess: x / sqrt(mean(x^2) + eps) * w): a constant head c at
+    position 0 becomes c / sqrt(c^2 + eps), rounded once to FP16 (numpy's
+    float16 conversion, an independent library routine, rounds it here)."""
+    B, S, Hq, Hkv, D, r, cap = 1, 1, 1, 1, 64, 64, 2
+    qkv = np.zeros((B, S, 3, D))
+    qkv[0, 0, 0], qkv[0, 0, 1], qkv[0, 0, 2] = 2.0, -1.0, 0.75
+    qkv = qkv.astype(np.float16).view(np.uint16)
+    cs = workloads.cos_sin_table(1e4, cap, r)      # row 0: the identity
+    ones = _w(np.ones(D))
+    for eps in (0.5, 3.0):
+        cache = workloads.sentinel_fill((B, 2, Hkv, cap, D))
+        qo = workloads.sentinel_fill((B, S, Hq, D))
+        oracle.continuous_qknorm(cs, np.array([1], dtype=np.int32), qkv, cache, qo, ones, ones,
+                                 eps, Hq, Hkv, oracle.NEOX)
+        want_q = np.float16(2.0 / math.sqrt(4.0 + eps))
+        want_k = np.float16(-1.0 / math.sqrt(1.0 + eps))
+        assert np.all(qo.view(np.float16) == want_q), eps
+        assert np.all(cache[0, 0, 0, 0].view(np.float16) == want_k), eps
+        assert np.array_equal(cache[0, 1, 0, 0], qkv[0, 0, 2])

@@ -80,3 +80,43 @@ def test_slot_mapping_gqa_heads():
     assert np.array_equal(kc[1, 1], k[0]) and np.array_equal(vc[1, 1], v[0])
     assert np.array_equal(kc[0, 0], k[1]) and np.array_equal(vc[0, 0], v[1])
     assert np.array_equal(qo, q)
+
+
+def test_slot_mapping_separate_strides():
+    """q, k and v each carry their own token stride (sglang rope_cache.py passes
+    q_stride_t, k_stride_t and v_stride_t separately). Here q and v are views
+    into two differently padded buffers and k is a plain array; every output
+    must still come from its own token's row."""
+    T, Hq, Hkv, D, r = 3, 2, 1, 16, 16
+    qbuf = coded_qkv(1, T, 5, D, tok_stride=1000)[0]          # stride 5 heads
+    vbuf = coded_qkv(1, T, 3, D, tok_stride=1000)[0] + 7      # stride 3 heads
+    q, v = qbuf[:, 1:1 + Hq], vbuf[:, 2:2 + Hkv]
+    k = np.ascontiguousarray(coded_qkv(1, T, Hkv, D, tok_stride=1000)[0] + 3)
+    assert len({q.strides[0], k.strides[0], v.strides[0]}) == 3
+    cs = identity_table(2, r)[0]
+    kc = workloads.sentinel_fill((1, 4, Hkv, D))
+    vc = workloads.sentinel_fill((1, 4, Hkv, D))
+    qo = workloads.sentinel_fill((T, Hq, D))
+    oracle.slot_mapping(cs, np.array([0, 0, 0], dtype=np.int64), q, k, v,
+                        np.array([2, 0, 3], dtype=np.int64), kc, vc, qo, None, oracle.NEOX)
+    assert np.array_equal(qo, q)
+    for t, slot in enumerate((2, 0, 3)):
+        assert np.array_equal(kc[0, slot], k[t]) and np.array_equal(vc[0, slot], v[t])
+    assert np.all(kc[0, 1] == SENT) and np.all(vc[0, 1] == SENT)
+
+
+@pytest.mark.parametrize("Hq,Hkv,r", [(3, 2, 16), (2, 1, 15)])
+def test_slot_mapping_rejects_invalid_dims(Hq, Hkv, r):
+    """Q heads in whole groups per KV head (QH_PER_KH = qh // kh) and an even
+    rotary width: anything else is an error that writes nothing."""
+    T, D = 2, 16
+    qkv = coded_qkv(1, T, Hq + 2 * Hkv, D)[0]
+    q, k, v = qkv[:, :Hq], qkv[:, Hq:Hq + Hkv], qkv[:, Hq + Hkv:]
+    cs = np.zeros((2, r), dtype=np.float32)
+    kc = workloads.sentinel_fill((1, 4, Hkv, D))
+    vc = workloads.sentinel_fill((1, 4, Hkv, D))
+    qo = workloads.sentinel_fill((T, Hq, D))
+    with pytest.raises(ValueError):
+        oracle.slot_mapping(cs, np.zeros(T, dtype=np.int64), q, k, v,
+                            np.arange(T, dtype=np.int64), kc, vc, qo, None, oracle.NEOX)
+    assert np.all(kc == SENT) and np.all(vc == SENT) and np.all(qo == SENT)
