@@ -127,23 +127,18 @@ struct GatherArgs {
 //                evict-last in L2 so the streaming traffic does not push
 //                them out.
 //   kPrefetch:   (with kPdl) before waiting for the previous grid, warm L2 with
-//                the thread's input vectors and the cos/sin row of the token's
-//                speculatively read position. Only L2 prefetches and
-//                L1-bypassing loads happen before the wait, so nothing stale can
-//                be consumed afterwards (L2 is the point of coherence), and a
-//                wrong speculative position only wastes one prefetch.
+//                the thread's input vectors and the token's position word.
+//                Only L2 prefetches happen before the wait: nothing is read
+//                into a register, so nothing stale can be consumed afterwards
+//                (L2 is the point of coherence) and no thread stalls on memory
+//                before the wait. (A blocking read of the position there, to
+//                prefetch the cos/sin row, cost a memory round trip per CTA:
+//                256-token decode 1.90 -> 2.12 us.)
 enum Policy : int { kPdl = 1, kStreamHint = 2, kTableKeep = 4, kPrefetch = 8 };
 
 __device__ __forceinline__ void prefetch_l2(const void* p)
 {
     asm volatile("prefetch.global.L2 [%0];" :: "l"(p));
-}
-
-__device__ __forceinline__ int load_int_l2(const int32_t* p)
-{
-    int v;
-    asm volatile("ld.global.cg.s32 %0, [%1];" : "=r"(v) : "l"(p));
-    return v;
 }
 
 struct L2Policies {
@@ -269,24 +264,6 @@ __device__ __forceinline__ void load_cos_sin(const float* row, int i, int r, flo
     c[4] = b.x; c[5] = b.y; c[6] = b.z; c[7] = b.w;
     s[0] = e.x; s[1] = e.y; s[2] = e.z; s[3] = e.w;
     s[4] = f.x; s[5] = f.y; s[6] = f.z; s[7] = f.w;
-}
-
-// L2 prefetch of exactly the cos/sin values load_cos_sin reads for item i
-// (a prefetch covers the 32-byte sector of its address; the row starts on a
-// 64-byte boundary, so NeoX's 8 cos and 8 sin floats are one sector each).
-template <int STYLE>
-__device__ __forceinline__ void prefetch_cos_sin(const float* row, int i, int r)
-{
-    const int h = r >> 1;
-    if (STYLE == kNeox) {
-        prefetch_l2(row + 8 * i);
-        prefetch_l2(row + h + 8 * i);
-    } else {
-        prefetch_l2(row + 4 * i);
-        prefetch_l2(row + 4 * i + (r >> 2));
-        prefetch_l2(row + h + 4 * i);
-        prefetch_l2(row + h + 4 * i + (r >> 2));
-    }
 }
 
 // NeoX: va holds dims 8i..8i+7 (first half), vb the partner dims 8i+r/2...;
@@ -439,7 +416,6 @@ __global__ void __launch_bounds__(256) rope_kv_token_kernel(const TokenArgs a)
     item_vectors<D>(i, a.r, va, vb);
     const uint16_t* tokIn = a.qkv + (size_t)tok * H * D;
 
-    int specPos = -1;  // speculative position (prefetch prologue only)
     if ((POL & kPdl) && (POL & kPrefetch)) {
 #pragma unroll
         for (int k = 0; k < IPT; ++k) {
@@ -450,29 +426,15 @@ __global__ void __launch_bounds__(256) rope_kv_token_kernel(const TokenArgs a)
                 prefetch_l2(p + 8 * vb);
             }
         }
-        if (MODE != kPacked && i < (a.r >> 4) && a.csSeq > 0) {
-            int pos = (MODE == kTree) ? load_int_l2(a.posIds + tok)
-                                      : load_int_l2(a.endLens + b) - a.S + s;
-            pos = min(max(pos, 0), a.csSeq - 1);
-            const int bc = (a.csBatch == 1) ? 0 : b;
-            prefetch_cos_sin<STYLE>(a.cosSin + ((size_t)bc * a.csSeq + pos) * a.r, i, a.r);
-            specPos = pos;
-        }
+        if (MODE != kPacked && threadIdx.x == 0)
+            prefetch_l2(MODE == kTree ? static_cast<const void*>(a.posIds + tok)
+                                      : static_cast<const void*>(a.endLens + b));
     }
     grid_dependency_sync<POL>();
     const L2Policies pol = make_policies<POL>();
     const bool rotItem = i < (a.r >> 4);
     const int bcRow = (a.csBatch == 1) ? 0 : b;
     float c[8], sn[8];
-    // After the wait every load sees the previous grid's writes. The cos/sin
-    // row of the speculative position is loaded now, in parallel with the
-    // position itself; it is kept only if the position turns out the same.
-    // (Measured on 256 decode tokens: plain 2.46 -> 2.38 us, QK-normalized
-    // 2.58 -> 2.48 us; the FP8 variant was slower with it, 2.17 -> 2.38 us,
-    // so it loads after the position.)
-    if (!FP8 && specPos >= 0 && rotItem)
-        load_cos_sin<STYLE, POL>(a.cosSin + ((size_t)bcRow * a.csSeq + specPos) * a.r, i, a.r, c,
-                                 sn, pol);
 
     // 1. this thread's QKV vectors (independent of the position chain)
     uint4 xa[IPT] = {}, xb[IPT] = {};
@@ -504,9 +466,8 @@ __global__ void __launch_bounds__(256) rope_kv_token_kernel(const TokenArgs a)
             return;  // skipped token: nothing written
     }
 
-    // 3. cos/sin for this thread's frequencies (unless the speculative
-    // position's row, already loaded, is the right one)
-    if (rotItem && (FP8 || pos != specPos)) {
+    // 3. cos/sin for this thread's frequencies
+    if (rotItem) {
         const float* row = a.cosSin + ((size_t)bcRow * a.csSeq + pos) * a.r;
         load_cos_sin<STYLE, POL>(row, i, a.r, c, sn, pol);
     }
@@ -776,8 +737,7 @@ __global__ void __launch_bounds__(256) rope_kv_slotmap_kernel(const SlotMapArgs 
     item_vectors<D>(i, a.r, va, vb);
 
     if ((POL & kPdl) && (POL & kPrefetch)) {
-        // L2 prefetches only (see kPrefetch): inputs, then the cos/sin row of
-        // the speculatively read position, clamped into the table
+        // L2 prefetches only (see kPrefetch): inputs and the position word
 #pragma unroll
         for (int k = 0; k < IPT; ++k) {
             const int item = item0 + k * blockDim.x;
@@ -790,12 +750,8 @@ __global__ void __launch_bounds__(256) rope_kv_slotmap_kernel(const SlotMapArgs 
                 prefetch_l2(p + 8 * vb);
             }
         }
-        if (i < (a.r >> 4) && a.csRows > 0) {
-            int64_t pos;
-            asm volatile("ld.global.cg.s64 %0, [%1];" : "=l"(pos) : "l"(a.positions + tok));
-            pos = pos < 0 ? 0 : (pos >= a.csRows ? a.csRows - 1 : pos);
-            prefetch_cos_sin<STYLE>(a.cosSin + pos * a.r, i, a.r);
-        }
+        if (threadIdx.x == 0)
+            prefetch_l2(a.positions + tok);
     }
     grid_dependency_sync<POL>();
     const L2Policies pol = make_policies<POL>();
