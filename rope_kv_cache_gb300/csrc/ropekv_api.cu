@@ -96,9 +96,15 @@ Shape pick_shape(int items, long long units, Work work = Work::kPlain)
 //     position -> cos/sin chain and the input reads off the critical path
 //     while the previous kernel in the stream drains (256 decode tokens:
 //     3.01 -> 2.47 us per launch), plus the residency cap below;
-//   * larger token and slot-mapping launches: dependent launch without the
-//     prologue (tree: 16.56 -> 16.17 us) when the grid has at most
-//     kPdlMaxCtas CTAs or its CTAs cover at least 256 items. The attribute
+//   * larger token and slot-mapping launches: dependent launch (tree: 16.56
+//     -> 16.17 us) when the grid has at most kPdlMaxCtas CTAs or its CTAs
+//     cover at least 256 items; plain continuous and packed launches also
+//     take the prefetch prologue (8192-token prefill 30.24 -> 29.99 us, 2048
+//     one-token decodes 8.93 -> 8.33 us, 4096-token prefill 16.15 -> 15.65
+//     us), the QK-normalized and FP8-cache ones do not (2048 tokens: 10.51 ->
+//     11.53 and 8.77 -> 9.74 us with it; 8192 tokens unchanged), nor do tree
+//     launches (unchanged) or slot-mapping ones (8192 tokens 30.36 -> 30.61
+//     us). The attribute
 //     caps the CTA launch rate near one CTA per nanosecond, which starves
 //     grids of many short CTAs (a 49 152-CTA prefill of 128-item CTAs: 29.9 ->
 //     49.8 us); a 256-item CTA moves ~16 KB, more than HBM delivers in a
@@ -209,8 +215,10 @@ int launch_token_variant(const TokenArgs& a, unsigned grid, const Shape& sh, cud
                 ropekv::rope_kv_token_kernel<D, STYLE, MODE, IPT, kPolSmall, NORM, FP8>>(
                 grid, sh.threads, st, a);
     }
+    constexpr int kPolMid =
+        (MODE != ropekv::kTree && !NORM && !FP8) ? (kPolPdl | ropekv::kPrefetch) : kPolPdl;
     if (pdl_allowed(grid, sh))
-        return launch_k(ropekv::rope_kv_token_kernel<D, STYLE, MODE, IPT, kPolPdl, NORM, FP8>,
+        return launch_k(ropekv::rope_kv_token_kernel<D, STYLE, MODE, IPT, kPolMid, NORM, FP8>,
                         grid, sh.threads, st, true, a);
     return launch_k(ropekv::rope_kv_token_kernel<D, STYLE, MODE, IPT, kPolLarge, NORM, FP8>, grid,
                     sh.threads, st, false, a);
