@@ -98,13 +98,14 @@ Shape pick_shape(int items, long long units, Work work = Work::kPlain)
 //     3.01 -> 2.47 us per launch), plus the residency cap below;
 //   * larger token and slot-mapping launches: dependent launch (tree: 16.56
 //     -> 16.17 us) when the grid has at most kPdlMaxCtas CTAs or its CTAs
-//     cover at least 256 items; plain continuous and packed launches also
-//     take the prefetch prologue (8192-token prefill 30.24 -> 29.99 us, 2048
-//     one-token decodes 8.93 -> 8.33 us, 4096-token prefill 16.15 -> 15.65
-//     us), the QK-normalized and FP8-cache ones do not (2048 tokens: 10.51 ->
-//     11.53 and 8.77 -> 9.74 us with it; 8192 tokens unchanged), nor do tree
-//     launches (unchanged) or slot-mapping ones (8192 tokens 30.36 -> 30.61
-//     us). The attribute
+//     cover at least 256 items; plain continuous, packed and slot-mapping
+//     launches also take the prefetch prologue (8192-token prefill 30.24 ->
+//     29.99 us, 2048 one-token decodes 8.93 -> 8.33 us, 4096-token prefill
+//     16.15 -> 15.65 us; slot mapping, 1024 one-token decodes 5.71 -> 5.39
+//     us, 8192 tokens 30.55 -> 30.47 us), the QK-normalized and FP8-cache
+//     ones do not (2048 tokens: 10.51 -> 11.53 and 8.77 -> 9.74 us with it;
+//     8192 tokens unchanged), nor do tree launches (1024 tokens 5.35 -> 5.55
+//     us with it, 4096 tokens 16.30 -> 16.25 us). The attribute
 //     caps the CTA launch rate near one CTA per nanosecond, which starves
 //     grids of many short CTAs (a 49 152-CTA prefill of 128-item CTAs: 29.9 ->
 //     49.8 us); a 256-item CTA moves ~16 KB, more than HBM delivers in a
@@ -398,9 +399,9 @@ int launch_slotmap(const ropekv::SlotMapArgs& a, bool gptj, unsigned grid, const
                     : launch_small<rope_kv_slotmap_kernel<D, ropekv::kNeox, 2, kPolSmall>>(
                           grid, sh.threads, st, a);
     if (pdl_allowed(grid, sh))
-        return gptj ? launch_k(rope_kv_slotmap_kernel<D, ropekv::kGptj, 2, kPolPdl>, grid,
+        return gptj ? launch_k(rope_kv_slotmap_kernel<D, ropekv::kGptj, 2, kPolPdl | ropekv::kPrefetch>, grid,
                                sh.threads, st, true, a)
-                    : launch_k(rope_kv_slotmap_kernel<D, ropekv::kNeox, 2, kPolPdl>, grid,
+                    : launch_k(rope_kv_slotmap_kernel<D, ropekv::kNeox, 2, kPolPdl | ropekv::kPrefetch>, grid,
                                sh.threads, st, true, a);
     return gptj ? launch_k(rope_kv_slotmap_kernel<D, ropekv::kGptj, 2, kPolLarge>, grid,
                            sh.threads, st, false, a)

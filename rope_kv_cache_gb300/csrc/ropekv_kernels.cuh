@@ -127,7 +127,8 @@ struct GatherArgs {
 //                evict-last in L2 so the streaming traffic does not push
 //                them out.
 //   kPrefetch:   (with kPdl) before waiting for the previous grid, warm L2 with
-//                the thread's input vectors and the token's position word.
+//                the thread's input vectors and the token's index words
+//                (end length and tree position, or position and slot).
 //                Only L2 prefetches happen before the wait: nothing is read
 //                into a register, so nothing stale can be consumed afterwards
 //                (L2 is the point of coherence) and no thread stalls on memory
@@ -426,9 +427,11 @@ __global__ void __launch_bounds__(256) rope_kv_token_kernel(const TokenArgs a)
                 prefetch_l2(p + 8 * vb);
             }
         }
-        if (MODE != kPacked && threadIdx.x == 0)
-            prefetch_l2(MODE == kTree ? static_cast<const void*>(a.posIds + tok)
-                                      : static_cast<const void*>(a.endLens + b));
+        if (MODE != kPacked && threadIdx.x == 0) {
+            prefetch_l2(a.endLens + b);
+            if (MODE == kTree)
+                prefetch_l2(a.posIds + tok);
+        }
     }
     grid_dependency_sync<POL>();
     const L2Policies pol = make_policies<POL>();
@@ -737,7 +740,7 @@ __global__ void __launch_bounds__(256) rope_kv_slotmap_kernel(const SlotMapArgs 
     item_vectors<D>(i, a.r, va, vb);
 
     if ((POL & kPdl) && (POL & kPrefetch)) {
-        // L2 prefetches only (see kPrefetch): inputs and the position word
+        // L2 prefetches only (see kPrefetch): inputs, the position and the slot
 #pragma unroll
         for (int k = 0; k < IPT; ++k) {
             const int item = item0 + k * blockDim.x;
@@ -750,8 +753,10 @@ __global__ void __launch_bounds__(256) rope_kv_slotmap_kernel(const SlotMapArgs 
                 prefetch_l2(p + 8 * vb);
             }
         }
-        if (threadIdx.x == 0)
+        if (threadIdx.x == 0) {
             prefetch_l2(a.positions + tok);
+            prefetch_l2(a.slots + tok);
+        }
     }
     grid_dependency_sync<POL>();
     const L2Policies pol = make_policies<POL>();
