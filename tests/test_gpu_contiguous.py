@@ -391,3 +391,28 @@ def test_large_launches_of_short_sequences(layout):
         if layout == "qknorm_one_token":
             case.norm = workloads.norm_weights(72, 128)
     check_contiguous(case)
+
+
+@pytest.mark.parametrize("mode,variant", [("continuous", "plain"), ("continuous", "norm"),
+                                          ("packed", "plain"), ("tree", "plain")])
+@pytest.mark.parametrize("tokens", [1023, 1024, 1025])
+def test_launch_policy_boundary(mode, variant, tokens):
+    """1023 tokens launch as decode-sized (prefetch prologue and residency
+    cap); 1024 and more switch to the larger launch's shape and policy, which
+    keeps the prologue for the plain continuous and packed calls only. Each
+    side of the switch gives the oracle's result (the FP8-cache call's
+    boundary is in test_gpu_fp8.py, the slot-mapping call's in
+    test_gpu_slotmap.py)."""
+    if mode == "continuous":
+        case = workloads.make_continuous(tokens, 1, 8, 2, 128, 128, 16, GPTJ, 5e5,
+                                         seed=5000 + tokens, name=f"edge{tokens}")
+        if variant == "norm":
+            case.norm = workloads.norm_weights(5000 + tokens, 128)
+    elif mode == "packed":
+        case = workloads.make_packed(1, tokens, 8, 2, 128, 64, tokens + 3, NEOX, 1e4,
+                                     seed=5100 + tokens, cs_seq=tokens, cache_init="sentinel",
+                                     name=f"edgep{tokens}")
+    else:
+        case = workloads.make_tree(tokens, 1, 8, 2, 128, 64, 64, GPTJ, 1e4, seed=5200 + tokens,
+                                   base_range=(0, 60), cs_seq=64, name=f"edget{tokens}")
+    check_contiguous(case)

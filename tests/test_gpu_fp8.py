@@ -86,11 +86,12 @@ def test_small_cases(idx):
         assert np.isin(o_cache[:, 0], [0x7E, 0xFE]).any()   # the case does saturate
 
 
-@pytest.mark.parametrize("tokens", [1, 153, 700])
+@pytest.mark.parametrize("tokens", [1, 153, 700, 1023, 1024, 1025])
 def test_small_launch_residency_caps(tokens):
-    """Decode-sized FP8 launches (two CTAs per token): 1 and 3 CTAs per SM, and
+    """Decode-sized FP8 launches (two CTAs per token): 1 and 3 CTAs per SM,
     700 tokens, 1400 CTAs, past the 8-per-SM limit above which no shared
-    memory is reserved."""
+    memory is reserved, and both sides of the 1024-token switch to the larger
+    launch's shape and policy."""
     case = workloads.make_continuous(tokens, 1, 8, 2, 128, 128, 16, NEOX, 5e5, seed=800 + tokens,
                                      name=f"fp8_caps{tokens}")
     case.fp8_scales = (0.05, 0.04)

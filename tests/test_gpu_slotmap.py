@@ -156,3 +156,23 @@ def test_three_different_token_strides(T):
     compare(to_host_bits(vc), o_vc, _rot_mask(D, r, False), "valueCache")
     compare(to_host_bits(qo), o_qo, (np.arange(D) < r)[None, None, :], "qOut")
     compare(to_host_bits(ko), o_ko, (np.arange(D) < r)[None, None, :], "kOut")
+
+
+@pytest.mark.parametrize("tokens", [1023, 1024, 1025])
+def test_launch_policy_boundary(tokens):
+    """One-token sequences on both sides of the 1024-token switch from the
+    decode-sized launch (prologue and residency cap) to the larger one
+    (prologue, no cap), with skipped slots and positions on each side."""
+    case = workloads.make_slotmap([1] * tokens, 8, 2, 128, 128, NEOX, 5e5, seed=600 + tokens,
+                                  block_size=4, num_blocks=tokens + 8,
+                                  start_range=(0, 1023), cs_rows=1024, name=f"smedge{tokens}")
+    rng = workloads.rng_for(tokens)
+    case.slots[rng.choice(tokens, size=9, replace=False)] = -1
+    case.positions[rng.choice(tokens, size=5, replace=False)] = 1024
+    g = [to_host_bits(x) if x is not None else None for x in _run(case, True)]
+    o = _oracle(case, True)
+    D, r = case.D, case.r
+    compare(g[0], o[0], _rot_mask(D, r, True), "keyCache")
+    compare(g[1], o[1], _rot_mask(D, r, False), "valueCache")
+    compare(g[2], o[2], (np.arange(D) < r)[None, None, :], "qOut")
+    compare(g[3], o[3], (np.arange(D) < r)[None, None, :], "kOut")
