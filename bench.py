@@ -109,13 +109,49 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def code_only(text: str) -> str:
+    """C/C++/CUDA source without its comments, the blank space of each line
+    collapsed and blank lines dropped: a comment edit leaves it unchanged,
+    any edit of the code (string literals, such as inline PTX, included)
+    changes it."""
+    out = []
+    i, n = 0, len(text)
+    while i < n:
+        ch = text[i]
+        if ch in "\"'":
+            j = i + 1
+            while j < n and text[j] != ch:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            out.append(" ")
+            i = n if j < 0 else j + 2
+        else:
+            out.append(ch)
+            i += 1
+    lines = (" ".join(line.split()) for line in "".join(out).splitlines())
+    return "\n".join(line for line in lines if line)
+
+
+KERNEL_SOURCES = ("rope_kv_cache_gb300/csrc/ropekv_kernels.cuh",
+                  "rope_kv_cache_gb300/csrc/ropekv_api.cu",
+                  "rope_kv_cache_gb300/csrc/ropekv_floor.cu")
+
+
 def source_sha():
+    """Hash of the kernel sources' code (comments and blank space aside): the
+    key that ties a profile capture to the kernels it measured."""
     import hashlib
     h = hashlib.sha256()
-    for rel in ("rope_kv_cache_gb300/csrc/ropekv_kernels.cuh", "rope_kv_cache_gb300/csrc/ropekv_api.cu",
-                "rope_kv_cache_gb300/csrc/ropekv_floor.cu"):
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            h.update(code_only(f.read()).encode("utf-8"))
+        h.update(b"\0")
     return h.hexdigest()[:16]
 
 

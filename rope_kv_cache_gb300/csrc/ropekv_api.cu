@@ -92,10 +92,11 @@ Shape pick_shape(int items, long long units, Work work = Work::kPlain)
 //     -> 21.10 us, QK-normalized decode 2.47 -> 2.45 us, tree 16.04 -> 16.01,
 //     the others within 0.2 %);
 //   * small (decode-sized) token and slot-mapping launches: programmatic
-//     dependent launch with the L2 prefetch prologue, which takes the
-//     position -> cos/sin chain and the input reads off the critical path
-//     while the previous kernel in the stream drains (256 decode tokens:
-//     3.01 -> 2.47 us per launch), plus the residency cap below;
+//     dependent launch with the L2 prefetch prologue, which brings the
+//     inputs and the index words into L2 while the previous kernel in the
+//     stream drains (256 decode tokens: 3.01 -> 1.90 us per launch with the
+//     residency cap below; the position -> cos/sin chain itself stays after
+//     the wait, one L2 round trip longer than a plain copy);
 //   * larger token and slot-mapping launches: dependent launch (tree: 16.56
 //     -> 16.17 us) when the grid has at most kPdlMaxCtas CTAs or its CTAs
 //     cover at least 256 items; plain continuous, packed and slot-mapping
