@@ -123,6 +123,28 @@ class ContiguousCase:
             per_tok += self.Hkv * self.D * 2      # K also rotated in place in qkv
         return per_tok * self.tokens
 
+    def positions(self) -> np.ndarray:
+        """[B, S] RoPE position of every token (packed: s; continuous: end - S
+        + s; tree: tokenPosIds)."""
+        if self.mode == "tree":
+            return np.asarray(self.pos_ids, dtype=np.int64)
+        s = np.arange(self.S, dtype=np.int64)[None, :]
+        if self.mode == "packed":
+            return np.repeat(s, self.B, axis=0)
+        return np.asarray(self.end_lens, dtype=np.int64)[:, None] - self.S + s
+
+    def algorithmic_bytes_distinct_rows(self) -> int:
+        """algorithmic_bytes with the cos/sin bytes counted once per distinct
+        table row a launch reads rather than once per token (tree siblings
+        share their position's row); tokens without a row in the table are
+        left out."""
+        pos = self.positions()
+        csB, csS = self.cos_sin.shape[:2]
+        table = np.broadcast_to(np.arange(self.B)[:, None] if csB > 1 else 0, pos.shape)
+        ok = (pos >= 0) & (pos < csS)
+        rows = len(set(zip(table[ok].tolist(), pos[ok].tolist())))
+        return self.algorithmic_bytes() - self.r * 4 * self.tokens + self.r * 4 * rows
+
 
 def norm_weights(seed: int, D: int, eps: float = 1e-6):
     """RMS-norm weights for Q and K heads, 1 + 0.1 N(0,1) rounded to FP16, and eps."""
