@@ -951,10 +951,11 @@ def main(argv=None):
                             "launches_timed": args.extra_steps, "kernel": _kernel_name(w),
                             "cache_per_ring_set": getattr(w, "caches_per_set", None),
                             "dram_bytes_per_launch_ncu": ncu_traffic(xname)}
-            if isinstance(w.case, workloads.ContiguousCase) and w.case.mode == "tree":
+            case = getattr(w, "case", None)     # the floor copy has no case
+            if isinstance(case, workloads.ContiguousCase) and case.mode == "tree":
                 # the same launch with each distinct cos/sin row counted once
                 # (siblings share their position's row)
-                bd = w.case.algorithmic_bytes_distinct_rows()
+                bd = case.algorithmic_bytes_distinct_rows()
                 extra[xname]["bytes_per_step_distinct_rows"] = bd
                 extra[xname]["effective_gbs_distinct_rows"] = bd / per / 1e9
             del w
