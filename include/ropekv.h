@@ -108,7 +108,7 @@ typedef struct {
  *   qkv     [B, S, Hq + 2*Hkv, headDim] FP16, heads ordered Q, K, V; read and
  *           written IN PLACE: Q and K heads are rotated, V heads are left as is.
  *   kvCache [B, 2, Hkv, kvCapacity, headDim] FP16, written: plane 0 = rotated K,
- *           plane 1 = V, at slots 0..S-1 ("from the start positions"); token s
+ *           plane 1 = V, at slots 0..S-1 (an empty cache fills from slot 0); token s
  *           uses cos/sin row s. Slots >= S are not touched.
  * Host errors: S > kvCapacity or S > cosSinSeqLen -> ROPEKV_ERR_CAPACITY.
  */
@@ -117,7 +117,8 @@ ROPEKV_API int rope_write_kv_packed(const float* cosSin, uint16_t* qkv, uint16_t
 
 /*
  * [ARW] launchApplyRopeWriteKVContinuousQAndKVCache: the cache already holds
- * tokens. kvCacheEndLens[b] is the end position after writing, so token s of
+ * tokens. kvCacheEndLens[b] is where sequence b ends once this call's tokens
+ * are written, so token s of
  * sequence b takes slot = position = kvCacheEndLens[b] - S + s.
  *   cosSin         [cosSinBatch, cosSinSeqLen, rotaryDim] FP32, read.
  *   kvCacheEndLens [B] INT32, read on the device.
@@ -136,10 +137,10 @@ ROPEKV_API int rope_write_kv_continuous(const float* cosSin, const int32_t* kvCa
  * rope_write_kv_continuous with pre-RoPE RMS normalization of Q and K fused in
  * (libmir-cuda execution.rs: qkv_postprocess normalizes Q and K with
  * query_norm / key_norm weights and an epsilon before RoPE, then the KV store
- * runs; "Dflash Runtime Kernels" calls its K input "k_normed"). Every Q head x
- * becomes x[d] / sqrt(mean_d' x[d']^2 + eps) * qNormWeight[d] (K heads with
- * kNormWeight), in FP32, before the rotation; the result is rounded to FP16
- * once. V is copied as bits. Dims >= rotaryDim of Q and K are normalized too.
+ * runs; "Dflash Runtime Kernels" takes its K input already normalized).
+ * Every Q head x becomes x[d] / sqrt(mean_d' x[d']^2 + eps) * qNormWeight[d]
+ * (K heads with kNormWeight), in FP32, before the rotation; the result is
+ * rounded to FP16 once. V is copied as bits. Dims >= rotaryDim of Q and K are normalized too.
  *   qNormWeight, kNormWeight  [headDim] FP16, read.
  *   eps                       >= 0.
  * Everything else as rope_write_kv_continuous.
@@ -170,7 +171,7 @@ ROPEKV_API int rope_write_kv_continuous_fp8(const float* cosSin, const int32_t* 
 /*
  * [ARW] launchApplyRopeWriteKVTreeDecoding: tree attention for speculative
  * decoding. As the continuous call, except that the RoPE position of token
- * (b, s) is tokenPosIds[b, s] ("position of token within sequence"); the cache
+ * (b, s) is tokenPosIds[b, s], the token's position in its sequence; the cache
  * slot stays kvCacheEndLens[b] - S + s, so sibling nodes that share a position
  * keep distinct slots.
  *   tokenPosIds [B, S] INT32, read on the device.

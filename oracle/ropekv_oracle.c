@@ -245,7 +245,7 @@ int ropekv_oracle_packed(const float* cosSin, uint16_t* qkv, uint16_t* kvCache,
     int H = Hq + 2 * Hkv;
     for (int b = 0; b < B; ++b) {
         for (int s = 0; s < S; ++s) {
-            int pos = s; /* empty cache: written from the start positions */
+            int pos = s; /* empty cache: the tokens fill it from slot 0 */
             int slot = s;
             uint16_t* tok = qkv + qkv_at(b, s, 0, S, H, D);
             const float* cs = cs_row_at(cosSin, b, pos, csBatch, csSeq, r);
@@ -266,9 +266,9 @@ int ropekv_oracle_continuous(const float* cosSin, const int32_t* kvCacheEndLens,
     int H = Hq + 2 * Hkv;
     for (int b = 0; b < B; ++b) {
         for (int s = 0; s < S; ++s) {
-            /* kvCacheEndLens is the end position after writing: the S new
-             * tokens take slots end-S .. end-1, and their positions equal
-             * their slots. */
+            /* kvCacheEndLens is where the sequence ends once the S new
+             * tokens are in: they take slots end-S .. end-1, and their
+             * positions equal their slots. */
             long long slot = (long long)kvCacheEndLens[b] - S + s;
             long long pos = slot;
             if (slot < 0 || slot >= cap || pos >= csSeq)

@@ -153,7 +153,8 @@ int ropekv_oracle_paged_fused(const uint16_t* kDelta, const uint16_t* vDelta, ui
 /* Pre-RoPE QK RMS normalization fused into the continuous call (libmir-cuda
  * execution.rs: qkv_postprocess normalizes Q and K with query_norm / key_norm
  * weights and epsilon, then applies RoPE, then the KV store; "Dflash Runtime
- * Kernels": kDelta is "k_normed, no RoPE"). Reading: each Q head x [D] becomes
+ * Kernels": its kDelta is K already normalized, not yet rotated). Reading:
+ * each Q head x [D] becomes
  *   x_hat[d] = x[d] / sqrt(mean_{d'} x[d']^2 + eps) * qNormWeight[d]
  * (K heads with kNormWeight), then RoPE on x_hat, rounded to FP16 once; V is
  * copied as bits. Weights are FP16 [D]. Placement and skips: as the continuous

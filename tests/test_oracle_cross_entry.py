@@ -1,9 +1,9 @@
 """Cross-checks between the oracle's entry points, over random shapes.
 
 The entry points come from different passages of the pages: the packed call
-writes "from the start positions" (TensorRT-Edge-LLM "Apply Rope Write KV",
-packed QKV), the continuous call takes kvCacheEndLens as "the end position
-after writing", the tree call takes the RoPE position from tokenPosIds, the
+fills an empty cache from slot 0 (TensorRT-Edge-LLM "Apply Rope Write KV",
+packed QKV), the continuous call takes kvCacheEndLens as where each sequence
+ends once the call's tokens are written, the tree call takes the RoPE position from tokenPosIds, the
 sglang-style call (rope_cache.py, fused_qk_rope_reshape_and_cache) takes a
 position and a flat slot per token, and the paged update ("Dflash Runtime
 Kernels") places rows through a page table. Where two of them must describe

@@ -10,8 +10,9 @@ holds exactly. Two kinds of cos/sin tables make the outputs readable by hand:
   rotate(x) * 2^k exactly, so each output also tells which table row was used.
 
 The expected slot maps are written out by hand from the pages:
-TensorRT-Edge-LLM "Apply Rope Write KV" (packed: slots from the start;
-continuous/tree: kvCacheEndLens is the end position after writing) and
+TensorRT-Edge-LLM "Apply Rope Write KV" (packed: an empty cache fills from
+slot 0; continuous/tree: kvCacheEndLens is where a sequence ends once the
+call's tokens are written) and
 "Dflash Runtime Kernels" (launchDFlashTargetKVCacheUpdate skip rules).
 Everything not listed must keep the sentinel.
 """
@@ -485,7 +486,7 @@ def test_paged_plane_boundaries():
 
 
 def test_packed_rejects_table_shorter_than_sequence():
-    """The packed call's positions are 0 .. S-1 ("from the start positions"),
+    """The packed call's positions are 0 .. S-1 (an empty cache, filled from 0),
     so a table with fewer than S rows cannot serve it: an error that writes
     nothing, even though the cache is long enough."""
     qkv = coded_qkv(1, 5, 4, 16)
